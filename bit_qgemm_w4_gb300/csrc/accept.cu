@@ -1,0 +1,547 @@
+// Softmax over the vocabulary and the acceptance rules of the verify step.
+//
+// Chain rule ("Speculative Decoding Clearly Explained", the cat-sat
+// walkthrough): accept draft i with probability min(1, p/q), left to right,
+// stop at the first rejection, draw the replacement from the normalised
+// positive part of p - q; if every draft is accepted the target supplies one
+// more token.  Tree rule ("Karpathy's Trick for Faster Local LLMs Finally Has
+// Proper Tooling", section "Issue with parallel draft generation"): verify the
+// tree and keep the longest valid path -- here greedily, a node is valid when
+// its token is the target's argmax for the row that scores it.
+//
+// Launch structure (two launches for the chain rule, one for the tree):
+//  * row_stats_kernel: grid (chunks, rows); each block reduces one V-chunk of
+//    one row to an online-softmax pair (max, sum exp(l - max)) -- one pass over
+//    the logits, coalesced.
+//  * accept_kernel: grid = V-chunks of the single row that is sampled.  Every
+//    block merges the per-row pairs, replays the (at most T) sequential
+//    accept tests itself, and sums its chunk of the residual max(0, p_j - q_j)
+//    (or of p_T); the last block to arrive (atomic counter, no waiting) does
+//    the inverse-CDF draw: it picks the chunk from the chunk sums and scans
+//    that chunk only.
+//  * tree_kernel: grid (chunks, T+1) argmax partials; the last block merges
+//    them and walks the tree.
+
+#include <cfloat>
+#include <cmath>
+
+#include "internal.hpp"
+
+namespace sv {
+namespace {
+
+constexpr int kBlock = 256;
+constexpr int kDevErrBadToken = 2;
+constexpr int kDevErrBadParent = 3;
+constexpr float kTieEps = 1e-4f;
+constexpr float kCdfEps = 1e-5f;
+
+struct MS {
+  float m, s;
+};
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) return {M, 0.f};
+  return {M, a.s * expf(a.m - M) + b.s * expf(b.m - M)};
+}
+
+__device__ __forceinline__ MS ms_add(MS a, float x) {
+  if (x > a.m) return {x, a.s * expf(a.m - x) + 1.f};
+  if (x == -INFINITY) return a;
+  return {a.m, a.s + expf(x - a.m)};
+}
+
+// Sum of a float over the block in a fixed order (deterministic).
+__device__ float block_sum(float v, float* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kBlock / 32; ++w) t += sh[w];
+  __syncthreads();
+  if (threadIdx.x == 0) sh[0] = t;
+  __syncthreads();
+  const float r = sh[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ MS block_ms(MS v, MS* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = ms_merge(v, w);
+  }
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  MS t{-INFINITY, 0.f};
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kBlock / 32; ++w) t = ms_merge(t, sh[w]);
+  __syncthreads();
+  if (threadIdx.x == 0) sh[0] = t;
+  __syncthreads();
+  const MS r = sh[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void chunk_range(int c, int nchunks, int V, int& lo, int& hi) {
+  const long long cs = ((long long)V + nchunks - 1) / nchunks;
+  lo = (int)min((long long)V, (long long)c * cs);
+  hi = (int)min((long long)V, (long long)(c + 1) * cs);
+}
+
+// ---------------------------------------------------------------- row stats
+
+__global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restrict__ logits, int V,
+                                                           int nchunks, float* __restrict__ stats) {
+  __shared__ MS sh[kBlock / 32];
+  const int c = blockIdx.x, row = blockIdx.y;
+  int lo, hi;
+  chunk_range(c, nchunks, V, lo, hi);
+  const float* l = logits + (long long)row * V;
+  MS a{-INFINITY, 0.f};
+  for (int v = lo + threadIdx.x; v < hi; v += kBlock) a = ms_add(a, __ldg(l + v));
+  a = block_ms(a, sh);
+  if (threadIdx.x == 0) {
+    stats[((long long)row * nchunks + c) * 2 + 0] = a.m;
+    stats[((long long)row * nchunks + c) * 2 + 1] = a.s;
+  }
+}
+
+__device__ __forceinline__ MS row_total(const float* stats, int row, int nchunks) {
+  MS t{-INFINITY, 0.f};
+  for (int c = 0; c < nchunks; ++c) {
+    const MS x{__ldcg(stats + ((long long)row * nchunks + c) * 2),
+               __ldcg(stats + ((long long)row * nchunks + c) * 2 + 1)};
+    t = ms_merge(t, x);
+  }
+  return t;
+}
+
+__global__ void __launch_bounds__(kBlock) softmax_norm_kernel(const float* __restrict__ logits,
+                                                              float* __restrict__ probs, int V,
+                                                              int nchunks,
+                                                              const float* __restrict__ stats) {
+  __shared__ MS tot;
+  const int c = blockIdx.x, row = blockIdx.y;
+  if (threadIdx.x == 0) tot = row_total(stats, row, nchunks);
+  __syncthreads();
+  const float M = tot.m, invZ = 1.f / tot.s;
+  int lo, hi;
+  chunk_range(c, nchunks, V, lo, hi);
+  const float* l = logits + (long long)row * V;
+  float* p = probs + (long long)row * V;
+  for (int v = lo + threadIdx.x; v < hi; v += kBlock) p[v] = expf(l[v] - M) * invZ;
+}
+
+// ---------------------------------------------------------------- chain accept
+
+struct AcceptArgs {
+  const float* logits;   // [T+1][V]
+  const float* q;        // [T][V]
+  const int32_t* drafts;
+  const float* u;        // [T+1]
+  int T, V;
+  int nstat;             // chunks of row_stats
+  const float* stats;
+  int nscan;             // blocks of accept_kernel == residual chunks
+  float* chunk_sums;     // [nscan]
+  int* counter;
+  int32_t* n_acc;
+  int32_t* tokens;
+  int32_t* flags;        // nullable
+  int* err;              // device error word
+};
+
+// Weight of token v in the final draw: residual max(0, p_j - q_j) at a
+// rejection (mode 0), p_j itself (mode 1: fallback when the residual has no
+// mass, only reachable through rounding), or p_T when all were accepted.
+struct DrawRow {
+  const float* l;
+  const float* q;   // null unless mode 0
+  float M, invZ;
+  int mode;
+  __device__ __forceinline__ float w(int v) const {
+    const float p = expf(__ldg(l + v) - M) * invZ;
+    return mode == 0 ? fmaxf(0.f, p - __ldg(q + v)) : p;
+  }
+};
+
+__global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
+  __shared__ float rowM[kMaxAcceptT + 1], rowInvZ[kMaxAcceptT + 1];
+  __shared__ float shf[kBlock / 32 + 1];
+  __shared__ int s_j, s_last, s_tok;
+  __shared__ float s_gap;
+  __shared__ int s_flag[kMaxAcceptT + 1];
+  __shared__ float s_pref[kScanBlocks + 1];
+  __shared__ float s_sub[kBlock + 1];
+
+  const int T = a.T, V = a.V;
+  for (int r = threadIdx.x; r <= T; r += kBlock) {
+    const MS t = row_total(a.stats, r, a.nstat);
+    rowM[r] = t.m;
+    rowInvZ[r] = 1.f / t.s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int j = T;
+    for (int i = 0; i < T; ++i) {
+      const int x = a.drafts[i];
+      float p = 0.f, qx = 1.f;
+      if (x >= 0 && x < V) {
+        p = expf(a.logits[(long long)i * V + x] - rowM[i]) * rowInvZ[i];
+        qx = a.q[(long long)i * V + x];
+      } else {
+        atomicCAS(a.err, 0, kDevErrBadToken);   // out-of-range draft: rejected, reported
+      }
+      const float r = qx == 0.f ? INFINITY : p / qx;
+      const float ui = a.u[i];
+      s_flag[i] = fabsf(ui - r) < kTieEps ? 1 : 0;
+      if (!(ui < fminf(1.f, r))) {
+        j = i;
+        break;
+      }
+    }
+    for (int i = j + 1; i < T; ++i) s_flag[i] = 0;
+    s_j = j;
+  }
+  __syncthreads();
+  const int j = s_j;
+  DrawRow dr;
+  dr.l = a.logits + (long long)j * V;
+  dr.q = j < T ? a.q + (long long)j * V : nullptr;
+  dr.M = rowM[j];
+  dr.invZ = rowInvZ[j];
+  dr.mode = j < T ? 0 : 1;
+
+  // this block's residual chunk sum
+  int lo, hi;
+  chunk_range(blockIdx.x, a.nscan, V, lo, hi);
+  float part = 0.f;
+  for (int v = lo + threadIdx.x; v < hi; v += kBlock) part += dr.w(v);
+  part = block_sum(part, shf);
+  if (threadIdx.x == 0) {
+    a.chunk_sums[blockIdx.x] = part;
+    __threadfence();
+    const int old = atomicAdd(a.counter, 1);
+    s_last = (old == a.nscan - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- last block: the single inverse-CDF draw
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (attempt == 1) {
+      // residual without mass (rounding only): draw from p_j instead
+      dr.mode = 1;
+      for (int c = 0; c < a.nscan; ++c) {
+        int l2, h2;
+        chunk_range(c, a.nscan, V, l2, h2);
+        float s = 0.f;
+        for (int v = l2 + threadIdx.x; v < h2; v += kBlock) s += dr.w(v);
+        s = block_sum(s, shf);
+        if (threadIdx.x == 0) a.chunk_sums[c] = s;
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      float acc = 0.f;
+      s_pref[0] = 0.f;
+      for (int c = 0; c < a.nscan; ++c) {
+        acc += __ldcg(a.chunk_sums + c);
+        s_pref[c + 1] = acc;
+      }
+    }
+    __syncthreads();
+    if (s_pref[a.nscan] > 0.f || attempt == 1) break;
+  }
+  const float Z = s_pref[a.nscan];
+  const float target = a.u[T] * Z;
+  if (threadIdx.x == 0) {
+    int cstar = -1;
+    for (int c = 0; c < a.nscan; ++c)
+      if (s_pref[c + 1] > target && s_pref[c + 1] > s_pref[c]) {
+        cstar = c;
+        break;
+      }
+    if (cstar < 0)   // rounding: last chunk with mass
+      for (int c = a.nscan - 1; c >= 0; --c)
+        if (s_pref[c + 1] > s_pref[c]) {
+          cstar = c;
+          break;
+        }
+    s_j = cstar < 0 ? 0 : cstar;   // reuse as the chosen chunk
+    s_tok = 0x7fffffff;
+    s_gap = 0.f;
+  }
+  __syncthreads();
+  const int cstar = s_j;
+  chunk_range(cstar, a.nscan, V, lo, hi);
+  const int len = hi - lo;
+  const int per = (len + kBlock - 1) / kBlock;
+  const int my_lo = min(hi, lo + threadIdx.x * per);
+  const int my_hi = min(hi, my_lo + per);
+  float sub = 0.f;
+  for (int v = my_lo; v < my_hi; ++v) sub += dr.w(v);
+  s_sub[threadIdx.x] = sub;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float acc = s_pref[cstar];
+    for (int t = 0; t < kBlock; ++t) {
+      const float x = s_sub[t];
+      s_sub[t] = acc;   // exclusive prefix
+      acc += x;
+    }
+  }
+  __syncthreads();
+  float cum = s_sub[threadIdx.x];
+  int cand = 0x7fffffff;
+  float cgap = 0.f;
+  for (int v = my_lo; v < my_hi; ++v) {
+    const float wv = dr.w(v);
+    const float nxt = cum + wv;
+    if (wv > 0.f && nxt > target) {
+      cand = v;
+      cgap = fminf(target - cum, nxt - target);
+      atomicMin(&s_tok, v);
+      break;
+    }
+    cum = nxt;
+  }
+  __syncthreads();
+  if (cand != 0x7fffffff && cand == s_tok) s_gap = cgap;
+  if (threadIdx.x == 0 && s_tok == 0x7fffffff) {
+    // rounding: last token with mass in the chosen chunk, reported as a near tie
+    int t = lo;
+    for (int v = hi - 1; v >= lo; --v)
+      if (dr.w(v) > 0.f) {
+        t = v;
+        break;
+      }
+    s_tok = t;
+    s_gap = 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.n_acc[0] = j;
+    for (int i = 0; i < j; ++i) a.tokens[i] = a.drafts[i];
+    a.tokens[j] = s_tok;
+    if (a.flags) {
+      for (int i = 0; i < T; ++i) a.flags[i] = s_flag[i];
+      a.flags[T] = (s_gap < kCdfEps * Z) ? 1 : 0;
+    }
+    *a.counter = 0;
+  }
+}
+
+// ---------------------------------------------------------------- greedy tree
+
+struct TreeArgs {
+  const float* logits;   // [T+1][V]
+  const int32_t* drafts;
+  const int32_t* parent;
+  int T, V, nchunks;
+  float* argval;         // [T+1][nchunks]
+  int* argidx;
+  int* counter;
+  int32_t* path_len;
+  int32_t* tokens;
+  int32_t* nodes;
+  int* err;
+};
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(kBlock) tree_kernel(TreeArgs a) {
+  __shared__ float shv[kBlock / 32];
+  __shared__ int shi[kBlock / 32];
+  __shared__ int s_last;
+  __shared__ int amax[kMaxAcceptT + 1];
+  __shared__ int depth[kMaxAcceptT];
+  __shared__ unsigned char ok[kMaxAcceptT];
+
+  const int c = blockIdx.x, row = blockIdx.y;
+  int lo, hi;
+  chunk_range(c, a.nchunks, a.V, lo, hi);
+  const float* l = a.logits + (long long)row * a.V;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = lo + threadIdx.x; v < hi; v += kBlock) {
+    const float x = __ldg(l + v);
+    if (better(x, v, bv, bi)) {
+      bv = x;
+      bi = v;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    shv[warp] = bv;
+    shi[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kBlock / 32; ++w)
+      if (better(shv[w], shi[w], bv, bi)) {
+        bv = shv[w];
+        bi = shi[w];
+      }
+    a.argval[row * a.nchunks + c] = bv;
+    a.argidx[row * a.nchunks + c] = bi;
+    __threadfence();
+    const int old = atomicAdd(a.counter, 1);
+    s_last = (old == (int)(gridDim.x * gridDim.y) - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int T = a.T;
+  for (int r = threadIdx.x; r <= T; r += kBlock) {
+    float v = -INFINITY;
+    int idx = 0x7fffffff;
+    for (int k = 0; k < a.nchunks; ++k) {
+      const float cv = __ldcg(a.argval + r * a.nchunks + k);
+      const int ci = __ldcg(a.argidx + r * a.nchunks + k);
+      if (better(cv, ci, v, idx)) {
+        v = cv;
+        idx = ci;
+      }
+    }
+    amax[r] = idx == 0x7fffffff ? 0 : idx;   // all-NaN row: token 0
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = -1;
+    for (int i = 0; i < T; ++i) {
+      int par = a.parent[i];
+      int row_i, d;
+      bool pok;
+      if (par < -1 || par >= i) {   // not a topological parent: node rejected, reported
+        atomicCAS(a.err, 0, kDevErrBadParent);
+        ok[i] = 0;
+        depth[i] = 1;
+        continue;
+      }
+      if (par < 0) {
+        pok = true;
+        row_i = 0;
+        d = 1;
+      } else {
+        pok = ok[par] != 0;
+        row_i = par + 1;
+        d = depth[par] + 1;
+      }
+      ok[i] = (pok && a.drafts[i] == amax[row_i]) ? 1 : 0;
+      depth[i] = d;
+      if (ok[i] && (best < 0 || d > depth[best])) best = i;
+    }
+    const int len = best < 0 ? 0 : depth[best];
+    int n = best;
+    for (int k = len - 1; k >= 0; --k) {
+      a.nodes[k] = n;
+      a.tokens[k] = a.drafts[n];
+      n = a.parent[n];
+    }
+    a.tokens[len] = amax[best + 1];
+    a.path_len[0] = len;
+    *a.counter = 0;
+  }
+}
+
+int stat_chunks(const spec_ctx* ctx, int rows, int V) {
+  long long want = (4LL * ctx->num_sms + rows - 1) / rows;
+  long long by_size = ((long long)V + 1023) / 1024;
+  long long c = want < by_size ? want : by_size;
+  if (c < 1) c = 1;
+  if (c > kAcceptChunks) c = kAcceptChunks;
+  return (int)c;
+}
+
+}  // namespace
+
+int launch_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows, int V,
+                   cudaStream_t s) {
+  const int nc = stat_chunks(ctx, rows, V);
+  dim3 g(nc, rows);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats);
+  int rc = check_cuda(cudaGetLastError(), "row_stats launch");
+  if (rc) return rc;
+  softmax_norm_kernel<<<g, kBlock, 0, s>>>(logits, probs, V, nc, ctx->acc_stats);
+  return check_cuda(cudaGetLastError(), "softmax_norm launch");
+}
+
+int launch_accept(spec_ctx* ctx, const float* logits, const float* q, const int32_t* drafts,
+                  const float* u, int T, int V, int32_t* n_acc, int32_t* tokens, int32_t* flags,
+                  cudaStream_t s) {
+  const int rows = T + 1;
+  const int nc = stat_chunks(ctx, rows, V);
+  dim3 g(nc, rows);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats);
+  int rc = check_cuda(cudaGetLastError(), "row_stats launch");
+  if (rc) return rc;
+  AcceptArgs a;
+  a.logits = logits;
+  a.q = q;
+  a.drafts = drafts;
+  a.u = u;
+  a.T = T;
+  a.V = V;
+  a.nstat = nc;
+  a.stats = ctx->acc_stats;
+  long long ns = ((long long)V + 1023) / 1024;
+  if (ns > kScanBlocks) ns = kScanBlocks;
+  if (ns < 1) ns = 1;
+  a.nscan = (int)ns;
+  a.chunk_sums = ctx->acc_chunks;
+  a.counter = ctx->acc_counters + 0;
+  a.n_acc = n_acc;
+  a.tokens = tokens;
+  a.flags = flags;
+  a.err = ctx->err;
+  accept_kernel<<<a.nscan, kBlock, 0, s>>>(a);
+  return check_cuda(cudaGetLastError(), "accept launch");
+}
+
+int launch_accept_tree(spec_ctx* ctx, const float* logits, const int32_t* drafts,
+                       const int32_t* parent, int T, int V, int32_t* path_len, int32_t* tokens,
+                       int32_t* nodes, cudaStream_t s) {
+  const int rows = T + 1;
+  TreeArgs a;
+  a.logits = logits;
+  a.drafts = drafts;
+  a.parent = parent;
+  a.T = T;
+  a.V = V;
+  a.nchunks = stat_chunks(ctx, rows, V);
+  a.argval = ctx->acc_argval;
+  a.argidx = ctx->acc_argmax;
+  a.counter = ctx->acc_counters + 1;
+  a.path_len = path_len;
+  a.tokens = tokens;
+  a.nodes = nodes;
+  a.err = ctx->err;
+  dim3 g(a.nchunks, rows);
+  tree_kernel<<<g, kBlock, 0, s>>>(a);
+  return check_cuda(cudaGetLastError(), "tree launch");
+}
+
+}  // namespace sv

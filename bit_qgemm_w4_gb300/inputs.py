@@ -68,7 +68,7 @@ class W4Weights:
     qcodes: np.ndarray   # uint8 [N][K/2]
     scales: np.ndarray   # float16 [K/g][N]
     zeros: np.ndarray    # uint8 [K/g][N/2]
-    raw_codes: np.ndarray  # uint8 [N][K] (unpacked, for tests only)
+    raw_codes: np.ndarray | None  # uint8 [N][K] (unpacked, for tests only)
     raw_zeros: np.ndarray  # uint8 [K/g][N] (unpacked, for tests only)
 
     @property
@@ -90,16 +90,23 @@ class W8Weights:
 
 
 def w4_weights(rng: np.random.Generator, N: int, K: int, group_size: int = 64,
-               scale_lo: float = 0.005, scale_hi: float = 0.02) -> W4Weights:
+               scale_lo: float = 0.005, scale_hi: float = 0.02,
+               keep_raw: bool = True) -> W4Weights:
     """int4 asymmetric group-quantised weights: codes and zero points uniform
-    on 0..15, fp16 scales uniform on [scale_lo, scale_hi]."""
+    on 0..15, fp16 scales uniform on [scale_lo, scale_hi].  With
+    keep_raw=False the packed code bytes are drawn directly (a uniform byte is
+    two independent uniform nibbles) and the unpacked codes are not kept."""
     assert K % group_size == 0 and K % 2 == 0 and N % 2 == 0
     G = K // group_size
-    codes = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
+    if keep_raw:
+        codes = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
+        packed = pack_nibbles(codes)
+    else:
+        codes = None
+        packed = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     zeros = rng.integers(0, 16, size=(G, N), dtype=np.uint8)
     scales = rng.uniform(scale_lo, scale_hi, size=(G, N)).astype(np.float16)
-    return W4Weights(N, K, group_size, pack_nibbles(codes), scales,
-                     pack_nibbles(zeros), codes, zeros)
+    return W4Weights(N, K, group_size, packed, scales, pack_nibbles(zeros), codes, zeros)
 
 
 def w8_weights(rng: np.random.Generator, N: int, K: int, group_size: int = 0,

@@ -1,0 +1,193 @@
+/*
+ * specverify.h -- C ABI of the speculative-decoding verification step on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The verify step scores a block of T drafted tokens in one target-model pass,
+ * so every low-bit weight read from memory is used for T tokens instead of one
+ * ("Speculative Decoding Clearly Explained", the cat-sat walkthrough; "Karpathy's
+ * Trick for Faster Local LLMs Finally Has Proper Tooling", section "Producing
+ * several tokens from one model pass": 16 rows of work instead of 1).  The pass
+ * is a group-quantised weight GEMM followed by the acceptance rule.
+ *
+ * Conventions for every entry point
+ *  - Status is returned by value: SPEC_OK (0) or a negative SPEC_ERR_* code.
+ *    Nothing is thrown across the ABI.  spec_last_error() returns a
+ *    thread-local text for the last failure on the calling thread.
+ *  - All tensor pointers are DEVICE pointers on the context's device, owned by
+ *    the caller.  They must stay valid until the work on `stream` completes.
+ *    Every pointer must be 16-byte aligned unless stated otherwise.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls only enqueue work; results are valid once the caller synchronises.
+ *  - Shapes and arguments are checked on the host before anything is launched;
+ *    a rejected call launches nothing.
+ *  - A context owns a device workspace (split-K partial sums, tile counters,
+ *    rotated activations, acceptance scratch) and a device error word.  One
+ *    context must not be used by two streams at the same time: calls that
+ *    overlap on the GPU would race on the workspace.
+ *  - Device-side failures (a bounded wait that timed out) set the context's
+ *    sticky error word; spec_sync_status() reports and clears it.
+ *
+ * Storage layouts ("Karpathy's Trick ...", section "How Uzu optimizes bytes
+ * and tokens per pass": 4-bit asymmetric Medium tier, 8-bit symmetric Large
+ * tier, one scale shared by every value of a group; the byte layouts are this
+ * library's own):
+ *   int4 codes   uint8 [N][K/2]   element k of output row n in the low nibble
+ *                                 of byte k/2 when k is even, high when odd
+ *   int4 scales  fp16  [K/g][N]   one row per quantisation group of g
+ *                                 consecutive k
+ *   int4 zeros   uint8 [K/g][N/2] uint4 zero points, low nibble = even n
+ *   int8 codes   int8  [N][K]     values -127..127 (-128 is read as -128)
+ *   int8 scales  fp16  [N] (g == 0, per output channel) or [K/g][N]
+ *   activations  bf16  [T][K]     row-major
+ *   outputs      bf16 or fp32 [T][N] row-major
+ *   dequantised weight: w[n][k] = (code - zero) * scale (int4),
+ *                       w[n][k] = code * scale (int8)
+ *   GEMM: y[t][n] = sum_k x[t][k] * w[n][k], fp32 accumulation.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_ctx spec_ctx;
+
+enum spec_status {
+  SPEC_OK = 0,
+  SPEC_ERR_ARG = -1,      /* null or misaligned pointer, bad enum value        */
+  SPEC_ERR_SHAPE = -2,    /* unsupported size or divisibility                  */
+  SPEC_ERR_ARCH = -3,     /* the device is not sm_103                          */
+  SPEC_ERR_CUDA = -4,     /* a CUDA runtime/driver call failed                 */
+  SPEC_ERR_OOM = -5,      /* workspace allocation failed or is too small       */
+  SPEC_ERR_TIMEOUT = -6,  /* a bounded device-side wait ran out (sticky)       */
+  SPEC_ERR_NUMERIC = -7   /* reserved: non-finite inputs                       */
+};
+
+enum spec_dtype { SPEC_DTYPE_BF16 = 0, SPEC_DTYPE_F32 = 1 };
+
+/* Library version, (major << 16) | minor. */
+int spec_version(void);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* spec_last_error(void);
+
+/* Create a context on `device` (must be an sm_103 GPU, else SPEC_ERR_ARCH).
+ * workspace_bytes = 0 picks the default (enough for T <= 64, K <= 32768 and
+ * any N up to 2^22).  The context allocates its workspace with cudaMalloc and
+ * zeroes it.  On success *out receives the context. */
+int spec_create(int device, size_t workspace_bytes, spec_ctx** out);
+
+/* Free the context and its workspace.  NULL is accepted. */
+int spec_destroy(spec_ctx* ctx);
+
+/* Synchronise `stream`, then read and clear the context's device error word.
+ * Returns SPEC_OK or the first device-side error recorded since the last call:
+ * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_ARG when a draft
+ * token (spec_accept) or parent index (spec_accept_tree) read on the device was
+ * out of range (that draft/node was treated as rejected).  After an error the
+ * split-K counters are re-zeroed so the context is usable again. */
+int spec_sync_status(spec_ctx* ctx, void* stream);
+
+/* W4A16 verify GEMM ("How Uzu optimizes bytes and tokens per pass": Medium
+ * checkpoint, 4-bit asymmetric integer weights).
+ *   y[t][n] = sum_k x'[t][k] * (code[n][k] - zero[k/g][n]) * scale[k/g][n]
+ * x' = x, or, when signs != NULL and hadamard_block > 0, the block random
+ * Hadamard rotation of x (see fwht_rotate; the weights are taken as stored
+ * already rotated).
+ * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size % 64 == 0 and
+ * K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
+ * The (code - zero) factor is exact in bf16 and each group's partial sum is
+ * scaled in fp32, so the only roundings are fp32 accumulation and the final
+ * store. */
+int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
+                const uint8_t* zeros, int group_size, const uint16_t* x, void* y,
+                int y_dtype, int T, int N, int K, const int8_t* signs,
+                int hadamard_block, void* stream);
+
+/* W8A16 verify GEMM ("How Uzu optimizes bytes and tokens per pass": Large
+ * checkpoint, 8-bit symmetric quantisation, no zero point).
+ *   y[t][n] = sum_k x'[t][k] * code[n][k] * scale
+ * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size % 64
+ * == 0).  Rotation and sizes as qgemm_w4a16, except N % 8 == 0 suffices. */
+int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
+                int group_size, const uint16_t* x, void* y, int y_dtype, int T,
+                int N, int K, const int8_t* signs, int hadamard_block,
+                void* stream);
+
+/* Block-diagonal random Hadamard rotation ("How Uzu optimizes bytes and tokens
+ * per pass": random sign flips applied before the mixing, +1/-1 entries and
+ * one overall scale, each block mixed on its own, exactly reversible):
+ *   y[t][bB:(b+1)B] = (1/sqrt(B)) * H_B * (s[bB:(b+1)B] .* x[t][bB:(b+1)B])
+ * H_B is the Sylvester Hadamard matrix in natural order.  B = block is a power
+ * of two in [32, 1024], K % B == 0, signs int8 [K] of +1/-1 (any nonzero
+ * negative value counts as -1).  x, y bf16 [T][K]; y may alias x.  fp32 math,
+ * one rounding to bf16.  1 <= T. */
+int fwht_rotate(spec_ctx* ctx, const uint16_t* x, uint16_t* y, int T, int K,
+                const int8_t* signs, int block, void* stream);
+
+/* Row softmax ("Speculative Decoding Clearly Explained": p is the target
+ * model's probability): probs[i][v] = exp(l[i][v] - max_i) / sum_w exp(l[i][w]
+ * - max_i) for rows x V fp32 logits.  1 <= rows <= 4096, 1 <= V <= 2^26.
+ * logits/probs need only 4-byte alignment. */
+int spec_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows,
+                 int V, void* stream);
+
+/* Chain acceptance ("Speculative Decoding Clearly Explained": accept draft i
+ * with probability min(1, p/q) left to right, stop at the first rejection,
+ * sample the replacement from normalize(max(0, p - q)); if every draft is
+ * accepted the target supplies one more token).
+ *   target_logits fp32 [T+1][V]: row i scores draft i, row T follows the last
+ *   draft_probs   fp32 [T][V]   (used as given, not renormalised)
+ *   draft_tokens  int32 [T]     in [0, V)
+ *   uniforms      fp32 [T+1]    in [0, 1): u[i] tests draft i, u[T] drives the
+ *                               single final draw (inverse CDF in ascending
+ *                               token order)
+ * Draft i is accepted iff u[i] < min(1, p_i(x_i) / q_i(x_i)) (q = 0 counts as
+ * +inf).  Outputs (device): n_accepted int32 [1]; out_tokens int32 [T+1], the
+ * first n_accepted+1 entries valid; near_tie_flags (nullable) int32 [T+1]:
+ * entry i < T is 1 when |u[i] - p/q| < 1e-4 at an evaluated position, entry T
+ * is 1 when the final draw lies within 1e-5 (relative) of a cumulative
+ * boundary.  0 <= T <= 256, 1 <= V <= 2^26.  Pointers need 4-byte alignment. */
+int spec_accept(spec_ctx* ctx, const float* target_logits,
+                const float* draft_probs, const int32_t* draft_tokens,
+                const float* uniforms, int T, int V, int32_t* n_accepted,
+                int32_t* out_tokens, int32_t* near_tie_flags, void* stream);
+
+/* Greedy tree acceptance ("Karpathy's Trick ...", section "Issue with parallel
+ * draft generation": the main model verifies the tree and accepts the longest
+ * valid path; "Local LLM 4x Faster ...": verify the entire tree at once).
+ *   target_logits fp32 [T+1][V]: row 0 scores the children of the root (the
+ *                  last committed token), row i+1 the children of node i
+ *   draft_tokens  int32 [T]; parent int32 [T] with parent[i] < i, -1 = child
+ *                  of the root
+ * Node i is accepted iff its parent is accepted (the root always is) and its
+ * token equals the largest-logit token of the row that scores it (ties go to
+ * the smallest token id).  The deepest accepted node wins (ties to the
+ * smallest node index).  Outputs (device): path_len int32 [1]; out_tokens
+ * int32 [T+1] = the path's tokens then the bonus token (the argmax of the row
+ * that follows the last path node, row 0 for an empty path); path_nodes
+ * int32 [T], the first path_len entries valid.  1 <= T <= 256,
+ * 1 <= V <= 2^26.  Pointers need 4-byte alignment. */
+int spec_accept_tree(spec_ctx* ctx, const float* target_logits,
+                     const int32_t* draft_tokens, const int32_t* parent, int T,
+                     int V, int32_t* path_len, int32_t* out_tokens,
+                     int32_t* path_nodes, void* stream);
+
+/* Dequantised weights as fp32 [N][K] (exact: (code - zero) * scale and
+ * code * scale both fit in fp32), for checking a packed checkpoint.  Layouts
+ * and size rules as the GEMMs (int4 additionally N % 2 == 0 only). */
+int qdequant_w4(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
+                const uint8_t* zeros, int group_size, int N, int K, float* w,
+                void* stream);
+int qdequant_w8(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
+                int group_size, int N, int K, float* w, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

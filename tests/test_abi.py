@@ -1,0 +1,48 @@
+"""The C ABI library builds, loads and exports every entry point that
+include/specverify.h declares; argument checks work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_qgemm_w4_gb300 as sv
+from bit_qgemm_w4_gb300 import build as svbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "specverify.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return sv.lib()
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared() == sorted(sv.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.spec_version() >= 1
+
+
+def test_null_context_is_rejected_without_touching_a_gpu(lib):
+    rc = lib.qgemm_w4a16(None, None, None, None, 64, None, None, 0, 16, 128, 64, None, 0, None)
+    assert rc == -1
+    assert b"null context" in lib.spec_last_error()
+    assert lib.spec_destroy(None) == 0
+
+
+def test_create_out_pointer_checked(lib):
+    assert lib.spec_create(0, 0, None) == -1

@@ -33,40 +33,44 @@ namespace {
 constexpr int kBlock = 256;
 constexpr int kDevErrBadToken = 2;
 constexpr int kDevErrBadParent = 3;
-constexpr float kTieEps = 1e-4f;
-constexpr float kCdfEps = 1e-5f;
+constexpr double kTieEps = 1e-4;   // |u - p/q| band reported as a near tie
+constexpr double kCdfEps = 1e-7;   // final draw within this fraction of a CDF boundary
 
+// Exponentials are fp32 (expf, <= 2 ulp); every sum over the vocabulary is
+// accumulated in fp64, so cumulative probabilities carry only the per-term
+// exponential error, well inside kCdfEps.
 struct MS {
-  float m, s;
+  float m;
+  double s;
 };
 
 __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   const float M = fmaxf(a.m, b.m);
-  if (M == -INFINITY) return {M, 0.f};
-  return {M, a.s * expf(a.m - M) + b.s * expf(b.m - M)};
+  if (M == -INFINITY) return {M, 0.0};
+  return {M, a.s * (double)expf(a.m - M) + b.s * (double)expf(b.m - M)};
 }
 
 __device__ __forceinline__ MS ms_add(MS a, float x) {
-  if (x > a.m) return {x, a.s * expf(a.m - x) + 1.f};
+  if (x > a.m) return {x, a.s * (double)expf(a.m - x) + 1.0};
   if (x == -INFINITY) return a;
-  return {a.m, a.s + expf(x - a.m)};
+  return {a.m, a.s + (double)expf(x - a.m)};
 }
 
-// Sum of a float over the block in a fixed order (deterministic).
-__device__ float block_sum(float v, float* sh) {
+// Sum over the block in a fixed order (deterministic).
+__device__ double block_sum(double v, double* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   __syncthreads();
   if (lane == 0) sh[warp] = v;
   __syncthreads();
-  float t = 0.f;
+  double t = 0.0;
   if (threadIdx.x == 0)
     for (int w = 0; w < kBlock / 32; ++w) t += sh[w];
   __syncthreads();
   if (threadIdx.x == 0) sh[0] = t;
   __syncthreads();
-  const float r = sh[0];
+  const double r = sh[0];
   __syncthreads();
   return r;
 }
@@ -81,7 +85,7 @@ __device__ MS block_ms(MS v, MS* sh) {
   __syncthreads();
   if (lane == 0) sh[warp] = v;
   __syncthreads();
-  MS t{-INFINITY, 0.f};
+  MS t{-INFINITY, 0.0};
   if (threadIdx.x == 0)
     for (int w = 0; w < kBlock / 32; ++w) t = ms_merge(t, sh[w]);
   __syncthreads();
@@ -101,13 +105,13 @@ __device__ __forceinline__ void chunk_range(int c, int nchunks, int V, int& lo, 
 // ---------------------------------------------------------------- row stats
 
 __global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restrict__ logits, int V,
-                                                           int nchunks, float* __restrict__ stats) {
+                                                           int nchunks, double* __restrict__ stats) {
   __shared__ MS sh[kBlock / 32];
   const int c = blockIdx.x, row = blockIdx.y;
   int lo, hi;
   chunk_range(c, nchunks, V, lo, hi);
   const float* l = logits + (long long)row * V;
-  MS a{-INFINITY, 0.f};
+  MS a{-INFINITY, 0.0};
   for (int v = lo + threadIdx.x; v < hi; v += kBlock) a = ms_add(a, __ldg(l + v));
   a = block_ms(a, sh);
   if (threadIdx.x == 0) {
@@ -116,10 +120,10 @@ __global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restri
   }
 }
 
-__device__ __forceinline__ MS row_total(const float* stats, int row, int nchunks) {
-  MS t{-INFINITY, 0.f};
+__device__ __forceinline__ MS row_total(const double* stats, int row, int nchunks) {
+  MS t{-INFINITY, 0.0};
   for (int c = 0; c < nchunks; ++c) {
-    const MS x{__ldcg(stats + ((long long)row * nchunks + c) * 2),
+    const MS x{(float)__ldcg(stats + ((long long)row * nchunks + c) * 2),
                __ldcg(stats + ((long long)row * nchunks + c) * 2 + 1)};
     t = ms_merge(t, x);
   }
@@ -129,12 +133,12 @@ __device__ __forceinline__ MS row_total(const float* stats, int row, int nchunks
 __global__ void __launch_bounds__(kBlock) softmax_norm_kernel(const float* __restrict__ logits,
                                                               float* __restrict__ probs, int V,
                                                               int nchunks,
-                                                              const float* __restrict__ stats) {
+                                                              const double* __restrict__ stats) {
   __shared__ MS tot;
   const int c = blockIdx.x, row = blockIdx.y;
   if (threadIdx.x == 0) tot = row_total(stats, row, nchunks);
   __syncthreads();
-  const float M = tot.m, invZ = 1.f / tot.s;
+  const float M = tot.m, invZ = (float)(1.0 / tot.s);
   int lo, hi;
   chunk_range(c, nchunks, V, lo, hi);
   const float* l = logits + (long long)row * V;
@@ -151,9 +155,9 @@ struct AcceptArgs {
   const float* u;        // [T+1]
   int T, V;
   int nstat;             // chunks of row_stats
-  const float* stats;
+  const double* stats;
   int nscan;             // blocks of accept_kernel == residual chunks
-  float* chunk_sums;     // [nscan]
+  double* chunk_sums;    // [nscan]
   int* counter;
   int32_t* n_acc;
   int32_t* tokens;
@@ -167,45 +171,47 @@ struct AcceptArgs {
 struct DrawRow {
   const float* l;
   const float* q;   // null unless mode 0
-  float M, invZ;
+  float M;
+  double invZ;
   int mode;
-  __device__ __forceinline__ float w(int v) const {
-    const float p = expf(__ldg(l + v) - M) * invZ;
-    return mode == 0 ? fmaxf(0.f, p - __ldg(q + v)) : p;
+  __device__ __forceinline__ double w(int v) const {
+    const double p = (double)expf(__ldg(l + v) - M) * invZ;
+    return mode == 0 ? fmax(0.0, p - (double)__ldg(q + v)) : p;
   }
 };
 
 __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
-  __shared__ float rowM[kMaxAcceptT + 1], rowInvZ[kMaxAcceptT + 1];
-  __shared__ float shf[kBlock / 32 + 1];
+  __shared__ float rowM[kMaxAcceptT + 1];
+  __shared__ double rowInvZ[kMaxAcceptT + 1];
+  __shared__ double shf[kBlock / 32 + 1];
   __shared__ int s_j, s_last, s_tok;
-  __shared__ float s_gap;
+  __shared__ double s_gap;
   __shared__ int s_flag[kMaxAcceptT + 1];
-  __shared__ float s_pref[kScanBlocks + 1];
-  __shared__ float s_sub[kBlock + 1];
+  __shared__ double s_pref[kScanBlocks + 1];
+  __shared__ double s_sub[kBlock + 1];
 
   const int T = a.T, V = a.V;
   for (int r = threadIdx.x; r <= T; r += kBlock) {
     const MS t = row_total(a.stats, r, a.nstat);
     rowM[r] = t.m;
-    rowInvZ[r] = 1.f / t.s;
+    rowInvZ[r] = 1.0 / t.s;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int j = T;
     for (int i = 0; i < T; ++i) {
       const int x = a.drafts[i];
-      float p = 0.f, qx = 1.f;
+      double p = 0.0, qx = 1.0;
       if (x >= 0 && x < V) {
-        p = expf(a.logits[(long long)i * V + x] - rowM[i]) * rowInvZ[i];
-        qx = a.q[(long long)i * V + x];
+        p = (double)expf(a.logits[(long long)i * V + x] - rowM[i]) * rowInvZ[i];
+        qx = (double)a.q[(long long)i * V + x];
       } else {
         atomicCAS(a.err, 0, kDevErrBadToken);   // out-of-range draft: rejected, reported
       }
-      const float r = qx == 0.f ? INFINITY : p / qx;
-      const float ui = a.u[i];
-      s_flag[i] = fabsf(ui - r) < kTieEps ? 1 : 0;
-      if (!(ui < fminf(1.f, r))) {
+      const double r = qx == 0.0 ? (double)INFINITY : p / qx;
+      const double ui = (double)a.u[i];
+      s_flag[i] = fabs(ui - r) < kTieEps ? 1 : 0;
+      if (!(ui < fmin(1.0, r))) {
         j = i;
         break;
       }
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
   // this block's residual chunk sum
   int lo, hi;
   chunk_range(blockIdx.x, a.nscan, V, lo, hi);
-  float part = 0.f;
+  double part = 0.0;
   for (int v = lo + threadIdx.x; v < hi; v += kBlock) part += dr.w(v);
   part = block_sum(part, shf);
   if (threadIdx.x == 0) {
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
       for (int c = 0; c < a.nscan; ++c) {
         int l2, h2;
         chunk_range(c, a.nscan, V, l2, h2);
-        float s = 0.f;
+        double s = 0.0;
         for (int v = l2 + threadIdx.x; v < h2; v += kBlock) s += dr.w(v);
         s = block_sum(s, shf);
         if (threadIdx.x == 0) a.chunk_sums[c] = s;
@@ -254,18 +260,18 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
       __syncthreads();
     }
     if (threadIdx.x == 0) {
-      float acc = 0.f;
-      s_pref[0] = 0.f;
+      double acc = 0.0;
+      s_pref[0] = 0.0;
       for (int c = 0; c < a.nscan; ++c) {
         acc += __ldcg(a.chunk_sums + c);
         s_pref[c + 1] = acc;
       }
     }
     __syncthreads();
-    if (s_pref[a.nscan] > 0.f || attempt == 1) break;
+    if (s_pref[a.nscan] > 0.0 || attempt == 1) break;
   }
-  const float Z = s_pref[a.nscan];
-  const float target = a.u[T] * Z;
+  const double Z = s_pref[a.nscan];
+  const double target = (double)a.u[T] * Z;
   if (threadIdx.x == 0) {
     int cstar = -1;
     for (int c = 0; c < a.nscan; ++c)
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
         }
     s_j = cstar < 0 ? 0 : cstar;   // reuse as the chosen chunk
     s_tok = 0x7fffffff;
-    s_gap = 0.f;
+    s_gap = 0.0;
   }
   __syncthreads();
   const int cstar = s_j;
@@ -290,28 +296,28 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
   const int per = (len + kBlock - 1) / kBlock;
   const int my_lo = min(hi, lo + threadIdx.x * per);
   const int my_hi = min(hi, my_lo + per);
-  float sub = 0.f;
+  double sub = 0.0;
   for (int v = my_lo; v < my_hi; ++v) sub += dr.w(v);
   s_sub[threadIdx.x] = sub;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float acc = s_pref[cstar];
+    double acc = s_pref[cstar];
     for (int t = 0; t < kBlock; ++t) {
-      const float x = s_sub[t];
+      const double x = s_sub[t];
       s_sub[t] = acc;   // exclusive prefix
       acc += x;
     }
   }
   __syncthreads();
-  float cum = s_sub[threadIdx.x];
+  double cum = s_sub[threadIdx.x];
   int cand = 0x7fffffff;
-  float cgap = 0.f;
+  double cgap = 0.0;
   for (int v = my_lo; v < my_hi; ++v) {
-    const float wv = dr.w(v);
-    const float nxt = cum + wv;
-    if (wv > 0.f && nxt > target) {
+    const double wv = dr.w(v);
+    const double nxt = cum + wv;
+    if (wv > 0.0 && nxt > target) {
       cand = v;
-      cgap = fminf(target - cum, nxt - target);
+      cgap = fmin(target - cum, nxt - target);
       atomicMin(&s_tok, v);
       break;
     }
@@ -323,12 +329,12 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
     // rounding: last token with mass in the chosen chunk, reported as a near tie
     int t = lo;
     for (int v = hi - 1; v >= lo; --v)
-      if (dr.w(v) > 0.f) {
+      if (dr.w(v) > 0.0) {
         t = v;
         break;
       }
     s_tok = t;
-    s_gap = 0.f;
+    s_gap = 0.0;
   }
   __syncthreads();
   if (threadIdx.x == 0) {

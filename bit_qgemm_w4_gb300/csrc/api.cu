@@ -114,8 +114,8 @@ WsLayout layout_for(int num_sms) {
   L.counters = take(sizeof(int) * (size_t)kMaxTiles);
   L.partials = take(sizeof(float) * (size_t)kPartialSlotFloats * L.slots);
   L.xrot = take(sizeof(uint16_t) * (size_t)kMaxT * kMaxK);
-  L.stats = take(sizeof(float) * 2 * (size_t)4096 * kAcceptChunks);
-  L.chunks = take(sizeof(float) * kScanBlocks);
+  L.stats = take(sizeof(double) * 2 * (size_t)4096 * kAcceptChunks);
+  L.chunks = take(sizeof(double) * kScanBlocks);
   L.argidx = take(sizeof(int) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
   L.argval = take(sizeof(float) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
   L.acc_counters = take(sizeof(int) * 16);
@@ -229,8 +229,8 @@ int spec_create(int device, size_t workspace_bytes, spec_ctx** out) {
   ctx->partials = reinterpret_cast<float*>(ctx->ws + L.partials);
   ctx->max_slots = L.slots;
   ctx->xrot = reinterpret_cast<uint16_t*>(ctx->ws + L.xrot);
-  ctx->acc_stats = reinterpret_cast<float*>(ctx->ws + L.stats);
-  ctx->acc_chunks = reinterpret_cast<float*>(ctx->ws + L.chunks);
+  ctx->acc_stats = reinterpret_cast<double*>(ctx->ws + L.stats);
+  ctx->acc_chunks = reinterpret_cast<double*>(ctx->ws + L.chunks);
   ctx->acc_argmax = reinterpret_cast<int*>(ctx->ws + L.argidx);
   ctx->acc_argval = reinterpret_cast<float*>(ctx->ws + L.argval);
   ctx->acc_counters = reinterpret_cast<int*>(ctx->ws + L.acc_counters);

@@ -59,8 +59,8 @@ struct spec_ctx {
   float* partials = nullptr;      // [max_slots][kPartialSlotFloats]
   int max_slots = 0;
   uint16_t* xrot = nullptr;       // [kMaxT][kMaxK] rotated activations
-  float* acc_stats = nullptr;     // [rows][kAcceptChunks][2] (max, sum) partials
-  float* acc_chunks = nullptr;    // [kScanBlocks] residual chunk sums
+  double* acc_stats = nullptr;    // [rows][kAcceptChunks][2] (max, sum) partials
+  double* acc_chunks = nullptr;   // [kScanBlocks] residual chunk sums
   int* acc_argmax = nullptr;      // [kMaxAcceptT+1][kAcceptChunks] argmax partial index
   float* acc_argval = nullptr;    // [kMaxAcceptT+1][kAcceptChunks] argmax partial value
   int* acc_counters = nullptr;    // [16] arrival counters of the acceptance kernels

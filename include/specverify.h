@@ -150,7 +150,7 @@ int spec_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows,
  * +inf).  Outputs (device): n_accepted int32 [1]; out_tokens int32 [T+1], the
  * first n_accepted+1 entries valid; near_tie_flags (nullable) int32 [T+1]:
  * entry i < T is 1 when |u[i] - p/q| < 1e-4 at an evaluated position, entry T
- * is 1 when the final draw lies within 1e-5 (relative) of a cumulative
+ * is 1 when the final draw lies within 1e-7 (relative) of a cumulative
  * boundary.  0 <= T <= 256, 1 <= V <= 2^26.  Pointers need 4-byte alignment. */
 int spec_accept(spec_ctx* ctx, const float* target_logits,
                 const float* draft_probs, const int32_t* draft_tokens,

@@ -194,7 +194,7 @@ def _inverse_cdf(weights: np.ndarray, u: float):
     return v, gap
 
 
-def spec_accept(logits, q, drafts, u, tie_eps: float = 1e-4, cdf_eps: float = 1e-5):
+def spec_accept(logits, q, drafts, u, tie_eps: float = 1e-4, cdf_eps: float = 1e-7):
     """Chain acceptance of T drafts.
 
     Inputs: target logits [T+1][V] (row i scores draft i, row T follows the

@@ -3,7 +3,7 @@ the fp64 oracle, through the C ABI.
 
 Bars: probabilities within 1e-5 absolute; accepted lengths and token ids
 bit-exact, except draws the oracle flags as near ties (|u - p/q| < 1e-4, or a
-final draw within 1e-5 of a cumulative boundary), which are counted and
+final draw within 1e-7 (relative) of a cumulative boundary), which are counted and
 reported separately; tree results bit-exact.
 """
 import json

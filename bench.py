@@ -1,0 +1,612 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one verify pass of a 9B-class decoder at T = 32 drafted tokens:
+36 layers of int4 asymmetric group-64 projections (fused q/k/v 4096->6144,
+o 4096->4096, fused gate/up 4096->24576, down 12288->4096), the int4 LM head
+(4096 -> 151936, fp32 logits), then the acceptance rule over 32 drafts on
+V = 151936 (softmax, min(1, p/q) tests, residual resample / bonus token).
+The synthetic draft distributions rotate over three acceptance levels
+(~0.3, ~0.6, ~0.9).  Weights (4.08 GB) are drawn on the device from a seeded
+generator; they exceed L2, so no step reuses another's cached weights.
+
+Printed: one JSON line.  `value` is algorithmic HBM bytes per step / device
+time per step (GB/s) with inputs resident; `e2e` is the same metric when
+every step also copies its inputs from pinned host memory and reads its
+result back; `t16` is the same stack at T = 16 without head and acceptance.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bit_qgemm_w4_gb300 import inputs  # noqa: E402
+
+T_MAIN, T_SMALL = 32, 16
+VOCAB = inputs.VOCAB_9B
+HIDDEN = 4096
+GROUP = 64
+ACCEPT_LEVELS = (0.3, 0.6, 0.9)
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "verify-step HBM GB/s (% of peak) and draft tokens scored/s at T=16/32, int4 9B-class"
+WORKLOAD = ("9B-class int4 g64 verify step, T=32: 36 layers (qkv 4096x6144, o 4096x4096, "
+            "gate_up 4096x24576, down 12288x4096) + LM head 4096x151936 (fp32 logits) + "
+            "softmax/accept over V=151936")
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes
+# ----------------------------------------------------------------------------
+
+def w4_gemm_bytes(T: int, N: int, K: int, g: int = GROUP, out_bytes: int = 2) -> int:
+    """Bytes a W4A16 GEMM must move: packed codes (0.5 B/weight), fp16 scales
+    and uint4 zeros per group, bf16 activations in, outputs out."""
+    return N * K // 2 + (K // g) * N * 2 + (K // g) * (N // 2) + T * K * 2 + T * N * out_bytes
+
+
+def stack_bytes(T: int) -> int:
+    return inputs.LAYERS_9B * sum(w4_gemm_bytes(T, N, K) for _, K, N in inputs.LAYER_9B)
+
+
+def head_bytes(T: int) -> int:
+    return w4_gemm_bytes(T, VOCAB, HIDDEN, out_bytes=4)
+
+
+def accept_bytes(T: int, V: int = VOCAB) -> int:
+    """Target logits of all T+1 rows once, plus the one draft-probability row
+    the final draw needs."""
+    return (T + 1) * V * 4 + V * 4
+
+
+def step_bytes(T: int = T_MAIN) -> int:
+    return stack_bytes(T) + head_bytes(T) + accept_bytes(T)
+
+
+def gemm_launches_per_step() -> int:
+    return inputs.LAYERS_9B * len(inputs.LAYER_9B) + 1
+
+
+# ----------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ----------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs_burst", "hbm_gbs", "hbm_GBps"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "measured"
+            if isinstance(d.get("hbm"), dict):
+                for key in ("burst_gbs", "gbs"):
+                    if key in d["hbm"]:
+                        return float(d["hbm"][key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "bit_qgemm_w4_gb300", "csrc", "qgemm.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(key: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(key)
+    except Exception:
+        return None
+    if not d or d.get("qgemm_cu_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (replicas only: each rank runs its own verify step)
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, value: float, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(layer_host, x_host, acc_host, budget_s: float = 12.0):
+    """Time the fp64 oracle on a bounded sample of the step: layer 0's GEMMs
+    in order until the time budget is spent (at least one), then the
+    acceptance rule on one sweep point.  Returns (GB/s, seconds, description)."""
+    import oracle
+    t0 = time.perf_counter()
+    done_bytes = 0
+    names = []
+    for (name, K, N), w, xb in zip(inputs.LAYER_9B, layer_host, x_host):
+        oracle.qgemm_w4a16(w["qcodes"], w["scales"], w["zeros"], GROUP, xb, T_MAIN, N, K)
+        done_bytes += w4_gemm_bytes(T_MAIN, N, K)
+        names.append(name)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    a = acc_host
+    oracle.spec_accept(a.logits, a.q, a.drafts, a.u)
+    done_bytes += accept_bytes(T_MAIN)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle (numpy fp64) on layer 0 {'+'.join(names)} at T=32 and one spec_accept "
+            f"over V={VOCAB}: {done_bytes / 1e6:.0f} MB of the step's {step_bytes() / 1e9:.2f} GB")
+    return done_bytes / dt / 1e9, dt, desc
+
+
+def host_layer0(seed: int = 4242):
+    """Layer-0 weights, activations and one acceptance input set on the host
+    (numpy generators; value distributions as the device stack)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    layer, xs = [], []
+    for _, K, N in inputs.LAYER_9B:
+        W = inputs.w4_weights(rng, N, K, GROUP, keep_raw=False)
+        layer.append({"qcodes": W.qcodes, "scales": W.scales, "zeros": W.zeros})
+        xs.append(inputs.activations(rng, T_MAIN, K))
+    sigma = inputs.fit_noise_for_acceptance(0.6, VOCAB, 3.0, seed=60)
+    acc = inputs.accept_inputs(rng, T_MAIN, VOCAB, logit_std=3.0, noise_std=sigma)
+    return layer, xs, acc
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+
+    world, rank, local = dist_setup()
+    svbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ctx = sv.Context(local)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20240 + rank)
+
+    # ---- weights and activations (device-resident)
+    layers = [[inputs.w4_weights_device(gen, N, K, dev, GROUP) for _, K, N in inputs.LAYER_9B]
+              for _ in range(inputs.LAYERS_9B)]
+    head = inputs.w4_weights_device(gen, VOCAB, HIDDEN, dev, GROUP)
+    xs = [[inputs.activations_device(gen, T_MAIN, K, dev) for _, K, _ in inputs.LAYER_9B]
+          for _ in range(inputs.LAYERS_9B)]
+    x_head = inputs.activations_device(gen, T_MAIN, HIDDEN, dev)
+    ys = [torch.empty((T_MAIN, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_9B]
+    logits_head = torch.empty((T_MAIN, VOCAB), dtype=torch.float32, device=dev)
+
+    # ---- acceptance inputs: three sweep points (host-generated, seeded)
+    acc_sets = []
+    for i, level in enumerate(ACCEPT_LEVELS):
+        sigma = inputs.fit_noise_for_acceptance(level, VOCAB, 3.0, seed=10 + i)
+        rng = np.random.default_rng(77 + i)
+        a = inputs.accept_inputs(rng, T_MAIN, VOCAB, logit_std=3.0, noise_std=sigma)
+        acc_sets.append({
+            "host": a, "sigma": sigma, "level": level,
+            "logits": torch.from_numpy(a.logits).to(dev), "q": torch.from_numpy(a.q).to(dev),
+            "drafts": torch.from_numpy(a.drafts).to(dev), "u": torch.from_numpy(a.u).to(dev),
+            "n": torch.zeros(1, dtype=torch.int32, device=dev),
+            "tok": torch.zeros(T_MAIN + 1, dtype=torch.int32, device=dev),
+        })
+
+    def gemm(w, x, y, T):
+        sv.qgemm_w4a16(ctx, w["qcodes"], w["scales"], w["zeros"], w["g"], x, y, T, w["N"], w["K"])
+
+    def stack(T):
+        for l in range(inputs.LAYERS_9B):
+            for j in range(len(inputs.LAYER_9B)):
+                gemm(layers[l][j], xs[l][j][:T], ys[j][:T], T)
+
+    def gemm_part():
+        stack(T_MAIN)
+        gemm(head, x_head, logits_head, T_MAIN)
+
+    def accept_part(i):
+        a = acc_sets[i]
+        sv.spec_accept(ctx, a["logits"], a["q"], a["drafts"], a["u"], T_MAIN, VOCAB, a["n"], a["tok"])
+
+    # ---- eager warm-up (also checks the device error word), then graphs
+    gemm_part()
+    for i in range(3):
+        accept_part(i)
+    stack(T_SMALL)
+    sv.spec_sync_status(ctx)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    g_gemm, g_acc, g_t16 = torch.cuda.CUDAGraph(), [torch.cuda.CUDAGraph() for _ in range(3)], \
+        torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_gemm, stream=side):
+            gemm_part()
+        for i in range(3):
+            with torch.cuda.graph(g_acc[i], stream=side):
+                accept_part(i)
+        with torch.cuda.graph(g_t16, stream=side):
+            stack(T_SMALL)
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        g_gemm.replay()
+        g_acc[i % 3].replay()
+        g_t16.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: full verify steps, inputs resident
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        evs[i][0].record()
+        g_gemm.replay()
+        evs[i][1].record()
+        g_acc[i % 3].replay()
+        evs[i][2].record()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    total_ms = evs[0][0].elapsed_time(evs[K - 1][2])
+    gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    acc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms_med = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+
+    # ---- T=16 stack (configs' T=16 verify GEMM pass)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K16 = max(K, 10)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K16):
+        g_t16.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t16_ms = e0.elapsed_time(e1) / K16
+    clocks = sampler.stop()
+    sv.spec_sync_status(ctx)
+
+    # ---- end to end: inputs copied from pinned host memory every step,
+    # result (accepted count + tokens) read back every step
+    pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+    h_x = [[pin(xs[l][j]) for j in range(len(inputs.LAYER_9B))] for l in range(inputs.LAYERS_9B)]
+    h_xh = pin(x_head)
+    h_acc = [{k: pin(a[k]) for k in ("logits", "q", "drafts", "u")} for a in acc_sets]
+    h_out = [torch.empty(1, dtype=torch.int32).pin_memory(),
+             torch.empty(T_MAIN + 1, dtype=torch.int32).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for row in h_x for t in row) + \
+        h_xh.numel() * h_xh.element_size() + \
+        sum(v.numel() * v.element_size() for v in h_acc[0].values())
+    d2h = 4 * (T_MAIN + 2)
+    K_e2e = max(10, min(K, 200))
+    e2e_evs = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e2e_evs[0].record()
+    for i in range(K_e2e):
+        for l in range(inputs.LAYERS_9B):
+            for j in range(len(inputs.LAYER_9B)):
+                xs[l][j].copy_(h_x[l][j], non_blocking=True)
+        x_head.copy_(h_xh, non_blocking=True)
+        a, ha = acc_sets[i % 3], h_acc[i % 3]
+        for k in ("logits", "q", "drafts", "u"):
+            a[k].copy_(ha[k], non_blocking=True)
+        g_gemm.replay()
+        g_acc[i % 3].replay()
+        h_out[0].copy_(a["n"], non_blocking=True)
+        h_out[1].copy_(a["tok"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()   # the host reads the result
+        _ = int(h_out[0][0])
+    e2e_evs[1].record()
+    torch.cuda.synchronize()
+    e2e_ms = e2e_evs[0].elapsed_time(e2e_evs[1]) / K_e2e
+    sv.spec_sync_status(ctx)
+
+    total_ms = dist_max(world, total_ms, dev)
+    e2e_ms = dist_max(world, e2e_ms, dev)
+    ms_per_step = total_ms / K
+    nbytes = step_bytes()
+    gemm_bytes = stack_bytes(T_MAIN) + head_bytes(T_MAIN)
+    peak, peak_kind = hbm_peak()
+    achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+    launches = gemm_launches_per_step()
+    accepted = []
+    for a in acc_sets:
+        accepted.append({"level": a["level"], "sigma": round(a["sigma"], 4),
+                         "n_accepted": int(a["n"].item())})
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        lay, xh, acc_h = host_layer0()
+        gbs, secs, desc = oracle_sample(lay, xh, acc_h, budget_s=args.cpu_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": desc + f"; {secs:.1f} s; numpy BLAS threads for the matmul, the rest "
+                                f"single-threaded"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC,
+            "value": round(world * nbytes / (ms_per_step * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int4 weights x bf16 activations, fp32 accumulate",
+            "data": "synthetic (seeded; weights drawn on device, value distributions of the "
+                    "configs)",
+            "config": {
+                "workload": WORKLOAD,
+                "T": T_MAIN, "layers": inputs.LAYERS_9B, "hidden": HIDDEN, "vocab": VOCAB,
+                "group_size": GROUP, "bytes_per_step": nbytes,
+                "acceptance_levels": list(ACCEPT_LEVELS),
+                "l2": "inputs larger than L2 (4.08 GB of weights per step)",
+                "parallelism": f"replicas x{world}",
+                "graph": "one CUDA graph per step part (GEMM stack+head, acceptance)",
+            },
+            "pct_of_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
+            "draft_tokens_scored_per_s": round(world * T_MAIN / (ms_per_step * 1e-3), 1),
+            "verify_step_ms_median": round(step_ms_med, 5),
+            "acceptance_ms": round(acc_ms, 5),
+            "acceptance_share": round(acc_ms / (gemm_ms + acc_ms), 4),
+            "accepted": accepted,
+            "t16": {
+                "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance)",
+                "ms_per_step": round(t16_ms, 5),
+                "value": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
+                "frac": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9 / peak, 4),
+                "draft_tokens_scored_per_s": round(T_SMALL / (t16_ms * 1e-3), 1),
+            },
+            "roofline": {
+                "kernel": "qgemm_kernel<W4, TPAD=32> (all 145 GEMM launches of a step)",
+                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                "peak_source": f"{peak_kind} HBM copy bandwidth" +
+                               (" (of fallback)" if peak_kind == "fallback" else " (of measured)"),
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic("qgemm_w4_t32_verify_step"),
+                "bytes_per_launch_avg": gemm_bytes // launches,
+                "launch_ms_avg": round(gemm_ms / launches, 6),
+            },
+            "cpu_baseline": cpu,
+            "e2e": {
+                "value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": K_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            },
+            "gpu_launches": K * (launches + 2),
+            "clocks": clocks,
+        }
+        print(json.dumps(out), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    lay, xh, acc_h = host_layer0()
+    levels = list(zip(inputs.LAYER_9B, lay, xh))
+
+    def sub(w, rows):
+        # output rows [r0, r1) of one int4 matrix (even bounds: zeros pack two rows)
+        r0, r1 = rows
+        return w["qcodes"][r0:r1], w["scales"][:, r0:r1], w["zeros"][:, r0 // 2:r1 // 2]
+
+    def gemm_rows(i, nrows):
+        (name, K, N), w, xb = levels[i % len(levels)]
+        r0 = (i // len(levels) * nrows) % N
+        r1 = min(N, r0 + nrows)
+        qc, sc, zr = sub(w, (r0, r1))
+        oracle.qgemm_w4a16(qc, sc, zr, GROUP, xb, T_MAIN, r1 - r0, K)
+        return w4_gemm_bytes(T_MAIN, r1 - r0, K)
+
+    # size each step so that warm-up + timed steps take about args.ref_seconds
+    t0 = time.perf_counter()
+    calib_bytes = gemm_rows(0, 512)
+    calib_s = time.perf_counter() - t0
+    per_step_s = args.ref_seconds / max(1, args.steps + args.warmup)
+    nrows = int(512 * per_step_s / max(calib_s, 1e-6)) // 2 * 2
+    nrows = max(32, min(nrows, 24576))
+
+    def one_step(i):
+        nbytes = gemm_rows(i, nrows)
+        if i % 16 == 15:
+            oracle.spec_accept(acc_h.logits, acc_h.q, acc_h.drafts, acc_h.u)
+            nbytes += accept_bytes(T_MAIN)
+        return nbytes
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(args.steps):
+        total += one_step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    gbs = total / dt / 1e9
+    sample = (f"each step: {nrows} output rows of one of layer 0's four int4 GEMMs at T=32, in "
+              f"rotation (qkv, o, gate_up, down), plus spec_accept over V=151936 every 16th "
+              f"step; throughput = algorithmic bytes of the sample / host time "
+              f"(calibration: 512 rows = {calib_bytes / 1e6:.1f} MB in {calib_s:.2f} s)")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "T": T_MAIN, "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_kernel_case(args):
+    """One W4A16 GEMM shape launched warm-up + steps times (for profiling one
+    kernel in isolation); prints its device time and achieved bandwidth."""
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    T, N, K = (int(v) for v in args.kernel_case.split(","))
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    # enough distinct matrices that consecutive launches do not hit in L2
+    copies = max(1, min(16, (256 << 20) // max(1, N * K // 2) + 1))
+    ws = [inputs.w4_weights_device(gen, N, K, dev, GROUP) for _ in range(copies)]
+    x = inputs.activations_device(gen, T, K, dev)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    for i in range(args.warmup):
+        w = ws[i % copies]
+        sv.qgemm_w4a16(ctx, w["qcodes"], w["scales"], w["zeros"], GROUP, x, y, T, N, K)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        w = ws[(args.warmup + i) % copies]
+        sv.qgemm_w4a16(ctx, w["qcodes"], w["scales"], w["zeros"], GROUP, x, y, T, N, K)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = w4_gemm_bytes(T, N, K)
+    print(json.dumps({"kernel_case": [T, N, K], "copies": copies, "ms_per_launch": round(ms, 6),
+                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes}), flush=True)
+    ctx.close()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle GEMM work in the CPU baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="host seconds the reference arm spends on warm-up + timed steps")
+    ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
+                    help="time one int4 GEMM shape in isolation instead of the verify step")
+    args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -373,7 +373,7 @@ int qdequant_w4(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales, co
   SV_TRY(check_ptr(scales, 2, "scales"));
   SV_TRY(check_ptr(zeros, 1, "zeros"));
   SV_TRY(check_ptr(w, 4, "w"));
-  if (N < 2 || N % 2 || K < 2 || K % 2 || group_size < 1 || K % group_size)
+  if (N < 2 || N % 2 || K < 8 || K % 8 || group_size < 1 || K % group_size)
     return set_error(SPEC_ERR_SHAPE, "bad int4 shape N=%d K=%d g=%d", N, K, group_size);
   DeviceGuard dg(ctx->device);
   if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);

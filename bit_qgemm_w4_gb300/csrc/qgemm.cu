@@ -42,8 +42,11 @@
 namespace sv {
 namespace {
 
-constexpr int kThreads = 192;      // warp 0: TMA, warp 1: TMEM owner + MMA, warps 2-5: dequant
+// warp 0: TMA producer; warp 1: TMEM owner + MMA issuer; warps 2-5: dequant
+// (one per TMEM lane quadrant); warps 6-9: epilogue (one per quadrant).
+constexpr int kThreads = 320;
 constexpr int kTmemCols = 256;     // two CTAs per SM share the 512 TMEM columns
+constexpr int kNumA = 4;           // TMEM ring of dequantised A tiles (32 columns each)
 
 template <int QUANT, int TPAD>
 struct Cfg {
@@ -62,12 +65,12 @@ struct Cfg {
   static constexpr int kSmemBudget = 110 * 1024;
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
-  static constexpr int kSlotCols = 32 + TPAD;                   // A (32 cols) + partial D
-  static constexpr int kTStagesFit = kTmemCols / kSlotCols;
-  static constexpr int kTStages = kTStagesFit > 4 ? 4 : kTStagesFit;
+  static constexpr int kPCols0 = 32 * kNumA;                    // P ring starts after the A ring
+  static constexpr int kNumPFit = (kTmemCols - kPCols0) / TPAD;
+  static constexpr int kNumP = kNumPFit > 8 ? 8 : kNumPFit;     // TMEM ring of stage partials
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
   static_assert(kStages >= 3, "pipeline too shallow");
-  static_assert(kTStages >= 2, "TMEM ring too shallow");
+  static_assert(kNumP >= 2, "TMEM partial ring too shallow");
 };
 
 struct Params {
@@ -77,8 +80,8 @@ struct Params {
   long long total;     // tiles * ks units
   void* y;
   int y_f32;
-  float* partials;
-  int* counters;
+  float* partials;     // split tiles: [first contributor CTA][TPAD][128] fp32, kept zeroed
+  int* counters;       // per tile arrival counters, kept zeroed
   int* err;
 };
 
@@ -93,8 +96,10 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int G) 
   return (int)c;
 }
 
-// int4: one thread dequantises one row's 64 codes (32 bytes) to bf16 pairs of
-// (code - zero), natural k order: a[j] holds k = 2j (low half), 2j+1 (high).
+// int4: one thread dequantises one row's 64 codes (32 bytes) to bf16 pairs
+// of (code - zero) in natural k order: a[j] holds k = 2j (low half) and
+// 2j+1 (high half).  Storage: byte j of each 4-byte word w holds
+// k = 8w+j in its low nibble and k = 8w+j+4 in its high nibble.
 __device__ __forceinline__ void dequant_row_w4(uint32_t code_addr, uint32_t row, uint32_t z,
                                                uint32_t (&a)[32]) {
   const uint32_t sw = (row >> 2) & 1u;                 // 32-byte swizzle: chunk ^= addr bit 7
@@ -102,17 +107,16 @@ __device__ __forceinline__ void dequant_row_w4(uint32_t code_addr, uint32_t row,
   const uint4 c1 = lds128(code_addr + ((1u ^ sw) << 4));
   const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   const uint32_t zz = (0x4300u | z) * 0x00010001u;     // bf16x2 (128 + z, 128 + z)
+  const uint32_t magic = 0x43434343u;                  // high byte of bf16 128.0
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const uint32_t q = words[w];
-    const uint32_t q4 = q >> 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // byte j of q holds k = 8w+2j (low nibble); byte j of q4 holds k = 8w+2j+1
-      const uint32_t t = __byte_perm(q, q4, 0x0400u + 0x0101u * j);
-      const uint32_t v = lop3_and_or(t, 0x000F000Fu, 0x43004300u);   // bf16x2 (128+c0, 128+c1)
-      a[4 * w + j] = sub_bf16x2(v, zz);                               // exact (c - z)
-    }
+    const uint32_t lo = words[w] & 0x0F0F0F0Fu;         // bytes: k0 k1 k2 k3
+    const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;  // bytes: k4 k5 k6 k7
+    // bf16x2 (128 + c_a, 128 + c_b) = bytes {c_a, 0x43, c_b, 0x43}
+    a[4 * w + 0] = sub_bf16x2(__byte_perm(lo, magic, 0x4140u), zz);
+    a[4 * w + 1] = sub_bf16x2(__byte_perm(lo, magic, 0x4342u), zz);
+    a[4 * w + 2] = sub_bf16x2(__byte_perm(hi, magic, 0x4140u), zz);
+    a[4 * w + 3] = sub_bf16x2(__byte_perm(hi, magic, 0x4342u), zz);
   }
 }
 
@@ -145,15 +149,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
+  constexpr int S = C::kStages, NA = kNumA, NP = C::kNumP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
+  uint8_t* ctrl = smem + S * C::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* a_ready = empty + C::kStages;
-  uint64_t* mma_done = a_ready + C::kTStages;
-  uint64_t* wg_bar = mma_done + C::kTStages;
+  uint64_t* empty = full + S;
+  uint64_t* a_full = empty + S;
+  uint64_t* a_empty = a_full + NA;
+  uint64_t* p_full = a_empty + NA;
+  uint64_t* p_empty = p_full + NP;
+  uint64_t* wg_bar = p_empty + NP;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* fix_flag = abort_flag + 1;
@@ -165,13 +172,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4 + 1);   // four dequant warps + one MMA commit
+      mbar_init(&empty[s], 4 + 1 + 4);   // dequant warps, MMA commit, epilogue warps
     }
-    for (int s = 0; s < C::kTStages; ++s) {
-      mbar_init(&a_ready[s], 4);
-      mbar_init(&mma_done[s], 1);
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < NP; ++s) {
+      mbar_init(&p_full[s], 1);
+      mbar_init(&p_empty[s], 4);
     }
     mbar_init(wg_bar, 4);
     *abort_flag = 0;
@@ -201,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (long long u = begin; u < end; ++u, ++i) {
         const int tile = (int)(u / p.ks);
         const int kst = (int)(u - (long long)tile * p.ks);
-        const int s = i % C::kStages;
-        if (!mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, abort_flag, p.err)) break;
+        const int s = i % S;
+        if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], C::kTx);
         tma_load_2d(st + C::kXOff, &tm_x, &full[s], kst * kStageK, 0);
@@ -214,9 +225,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (*abort_flag) {
         // drain copies still in flight into this CTA's shared memory
-        for (int j = (i > C::kStages ? i - C::kStages : 0); j < i; ++j) {
+        for (int j = (i > S ? i - S : 0); j < i; ++j) {
           volatile int no_abort = 0;
-          mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, &no_abort, nullptr, kDrainLimitNs);
+          mbar_wait(&full[j % S], (j / S) & 1, &no_abort, nullptr, kDrainLimitNs);
         }
       }
     }
@@ -226,37 +237,65 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
       int i = 0;
       for (long long u = begin; u < end; ++u, ++i) {
-        const int s = i % C::kStages;
-        const int ts = i % C::kTStages;
-        if (!mbar_wait(&full[s], (i / C::kStages) & 1, abort_flag, p.err)) break;
-        if (!mbar_wait(&a_ready[ts], (i / C::kTStages) & 1, abort_flag, p.err)) break;
+        const int s = i % S, sa = i % NA, sp = i % NP;
+        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&a_full[sa], (i / NA) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&p_empty[sp], ((i / NP) & 1) ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t a_col = tbase + ts * C::kSlotCols;
-        const uint32_t d_col = a_col + 32;
+        const uint32_t a_col = tbase + sa * 32;
+        const uint32_t d_col = tbase + C::kPCols0 + sp * TPAD;
         const uint64_t bdesc = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
           mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&mma_done[ts]);
+        mma_commit(&a_empty[sa]);
+        mma_commit(&p_full[sp]);
         mma_commit(&empty[s]);
       }
       if (*abort_flag && i > 0) {
         volatile int no_abort = 0;
         const int j = i - 1;
-        mbar_wait(&mma_done[j % C::kTStages], (j / C::kTStages) & 1, &no_abort, nullptr,
-                  kDrainLimitNs);
+        mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
       }
     }
-  } else {
-    // ------------------------------------------------------------ dequant + epilogue
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ dequant
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     const int m = q * 32 + lane;             // weight row inside the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const int first_tile = (int)(begin / p.ks);
+    int i = 0;
+    for (long long u = begin; u < end; ++u, ++i) {
+      const int s = i % S, sa = i % NA;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err))) break;
+      const uint8_t* st = smem + s * C::kStageBytes;
+      uint32_t a[32];
+      if constexpr (QUANT == kW4) {
+        const uint32_t zb = st[C::kZeroOff + (m >> 1)];
+        const uint32_t z = (zb >> ((m & 1) * 4)) & 0xFu;
+        dequant_row_w4(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, z, a);
+      } else {
+        dequant_row_w8(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, a);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&a_empty[sa], ((i / NA) & 1) ^ 1, abort_flag, p.err)))
+        break;
+      tc_fence_after();
+      tmem_st_32x32b_x32(tbase + lane_base + sa * 32, a);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[sa]);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t wg_phase = 0;
-
     auto wg_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(wg_bar);
@@ -268,86 +307,56 @@ __global__ void __launch_bounds__(kThreads, 2)
     float acc[TPAD];
 #pragma unroll
     for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-
-    // Add scale * partial(stage j) into acc; false on abort.
-    auto consume = [&](int j, float sc) -> bool {
-      const int ts = j % C::kTStages;
-      bool ok = mbar_wait(&mma_done[ts], (j / C::kTStages) & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      tc_fence_after();
-      uint32_t r[TPAD / 16][16];
-      const uint32_t d_addr = tbase + lane_base + ts * C::kSlotCols + 32;
-#pragma unroll
-      for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, r[h]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < TPAD / 16; ++h)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) acc[h * 16 + c] = fmaf(sc, __uint_as_float(r[h][c]), acc[h * 16 + c]);
-      return true;
-    };
-
     bool ok = true;
     int i = 0;
     long long u = begin;
-    int pend = -1;
-    float pend_scale = 0.f;
     while (ok && u < end) {
       const int tile = (int)(u / p.ks);
       const long long tile_first = (long long)tile * p.ks;
       const long long seg_end = min(end, tile_first + p.ks);
       const bool whole_tile = (u == tile_first) && (seg_end == tile_first + p.ks);
       for (; u < seg_end; ++u, ++i) {
-        const int s = i % C::kStages;
-        const int ts = i % C::kTStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / C::kStages) & 1, abort_flag, p.err));
+        const int s = i % S, sp = i % NP;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err));
         if (!ok) break;
-        const uint8_t* st = smem + s * C::kStageBytes;
-        const float sc = __half2float(reinterpret_cast<const __half*>(st + C::kScaleOff)[m]);
-        uint32_t a[32];
-        if constexpr (QUANT == kW4) {
-          const uint32_t zb = st[C::kZeroOff + (m >> 1)];
-          const uint32_t z = (zb >> ((m & 1) * 4)) & 0xFu;
-          dequant_row_w4(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, z, a);
-        } else {
-          dequant_row_w8(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, a);
-        }
+        const float sc = __half2float(
+            reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff)[m]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        // The slot's previous partial (stage i - kTStages) was consumed at
-        // iteration i - kTStages + 1 <= i - 1, so A and D may be overwritten.
-        tmem_st_32x32b_x32(tbase + lane_base + ts * C::kSlotCols, a);
-        tmem_wait_st();
+        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (i / NP) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * TPAD;
+#pragma unroll
+        for (int h = 0; h < TPAD / 16; ++h) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(d_addr + h * 16, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            acc[h * 16 + c] = fmaf(sc, __uint_as_float(r[c]), acc[h * 16 + c]);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_ready[ts]);
-        if (pend >= 0) {
-          ok = consume(pend, pend_scale);
-          if (!ok) break;
-        }
-        pend = i;
-        pend_scale = sc;
+        if (lane == 0) mbar_arrive(&p_empty[sp]);
       }
       if (!ok) break;
-      if (pend >= 0) {
-        ok = consume(pend, pend_scale);
-        if (!ok) break;
-        pend = -1;
-      }
 
       // ---- segment epilogue
       const int n = tile * kTileM + m;
       bool store = whole_tile;
       if (!whole_tile) {
-        const int slot = 2 * (int)blockIdx.x + (tile == first_tile ? 0 : 1);
-        float* w = p.partials + (size_t)slot * kPartialSlotFloats;
+        // Split tile: add this CTA's partial into the tile's fp32 slot (keyed
+        // by the tile's first contributor, unique per split tile); the last
+        // contributor to arrive converts the sum and clears the slot.
+        const int c_first = cta_of_unit(tile_first, p.total, G);
+        const int c_last = cta_of_unit(tile_first + p.ks - 1, p.total, G);
+        float* slot = p.partials + (size_t)c_first * kPartialSlotFloats;
 #pragma unroll
-        for (int t = 0; t < TPAD; ++t) w[t * kTileM + m] = acc[t];
+        for (int t = 0; t < TPAD; ++t) red_add_f32(slot + t * kTileM + m, acc[t]);
         __threadfence();
         ok = wg_sync();
         if (!ok) break;
-        const int c_first = cta_of_unit(tile_first, p.total, G);
-        const int c_last = cta_of_unit(tile_first + p.ks - 1, p.total, G);
         if (q == 0 && lane == 0) {
           const int old = atomicAdd(&p.counters[tile], 1);
           *fix_flag = (old == c_last - c_first) ? 1 : 0;
@@ -358,13 +367,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (store) {
           __threadfence();
 #pragma unroll
-          for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int c_first_tile = (int)(unit_begin(c, p.total, G) / p.ks);
-            const int cs = 2 * c + (c_first_tile == tile ? 0 : 1);
-            const float* wr = p.partials + (size_t)cs * kPartialSlotFloats;
-#pragma unroll
-            for (int t = 0; t < TPAD; ++t) acc[t] += __ldcg(wr + t * kTileM + m);
+          for (int t = 0; t < TPAD; ++t) {
+            acc[t] = __ldcg(slot + t * kTileM + m);
+            __stcg(slot + t * kTileM + m, 0.f);
           }
           if (q == 0 && lane == 0) atomicExch(&p.counters[tile], 0);
         }
@@ -441,7 +446,7 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.err = ctx->err;
   long long G = 2LL * ctx->num_sms;
   if (G > p.total) G = p.total;
-  if (2 * G > ctx->max_slots) return set_error(SPEC_ERR_OOM, "workspace has too few partial slots");
+  if (G > ctx->max_slots) return set_error(SPEC_ERR_OOM, "workspace has too few partial slots");
 
   static std::atomic<uint32_t> attr_done{0};   // per instantiation, one bit per device
   const uint32_t bit = ctx->device < 32 ? (1u << ctx->device) : 0u;

@@ -10,8 +10,9 @@ of the verify step, not part of it.
 
 Storage layouts (shared by the C ABI and the oracle):
 
-* int4 codes    uint8  [N][K/2]   element k of row n in the low nibble of byte
-                                   k/2 when k is even, the high nibble when odd
+* int4 codes    uint8  [N][K/2]   each 4-byte word w of a row holds k = 8w..8w+7:
+                                   byte 4w+j carries k = 8w+j in its low nibble and
+                                   k = 8w+j+4 in its high nibble (j = 0..3)
 * int4 scales   fp16   [K/g][N]   group-major (one row per quantisation group)
 * int4 zeros    uint8  [K/g][N/2] uint4 zero points, two output rows per byte,
                                    low nibble = even n
@@ -44,6 +45,18 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns (uint16) to float32 exactly."""
     b = np.ascontiguousarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def pack_w4_codes(codes: np.ndarray) -> np.ndarray:
+    """Pack uint4 codes [..., K] (K % 8 == 0) into the int4 code layout: in
+    each group of eight consecutive k, byte j (j = 0..3) holds element j in
+    its low nibble and element j+4 in its high nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    K = c.shape[-1]
+    assert K % 8 == 0
+    g = c.reshape(c.shape[:-1] + (K // 8, 8))
+    packed = (g[..., 0:4] & 0xF) | ((g[..., 4:8] & 0xF) << 4)
+    return packed.reshape(c.shape[:-1] + (K // 2,)).astype(np.uint8)
 
 
 def pack_nibbles(vals: np.ndarray) -> np.ndarray:
@@ -96,11 +109,11 @@ def w4_weights(rng: np.random.Generator, N: int, K: int, group_size: int = 64,
     on 0..15, fp16 scales uniform on [scale_lo, scale_hi].  With
     keep_raw=False the packed code bytes are drawn directly (a uniform byte is
     two independent uniform nibbles) and the unpacked codes are not kept."""
-    assert K % group_size == 0 and K % 2 == 0 and N % 2 == 0
+    assert K % group_size == 0 and K % 8 == 0 and N % 2 == 0
     G = K // group_size
     if keep_raw:
         codes = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
-        packed = pack_nibbles(codes)
+        packed = pack_w4_codes(codes)
     else:
         codes = None
         packed = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
@@ -267,3 +280,39 @@ VOCAB_9B = 151936
 LAYER_27B = (("qkv", 5120, 7168), ("o", 5120, 5120), ("gate_up", 5120, 34816),
              ("down", 17408, 5120))
 LAYERS_27B = 64
+
+
+# ----------------------------------------------------------------------------
+# device-resident stacks (benchmark sizes; drawn on the GPU from a seeded
+# torch generator, same value distributions as the numpy generators above)
+# ----------------------------------------------------------------------------
+
+def w4_weights_device(gen, N: int, K: int, device, group_size: int = 64,
+                      scale_lo: float = 0.005, scale_hi: float = 0.02) -> dict:
+    """int4 weights drawn on the device: packed code bytes and packed zero
+    bytes uniform on 0..255 (two independent uniform nibbles each), fp16
+    scales uniform on [scale_lo, scale_hi]."""
+    import torch
+    G = K // group_size
+    qcodes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=device, generator=gen)
+    zeros = torch.randint(0, 256, (G, N // 2), dtype=torch.uint8, device=device, generator=gen)
+    scales = (torch.rand((G, N), device=device, generator=gen) * (scale_hi - scale_lo)
+              + scale_lo).to(torch.float16)
+    return {"N": N, "K": K, "g": group_size, "qcodes": qcodes, "scales": scales, "zeros": zeros}
+
+
+def w8_weights_device(gen, N: int, K: int, device, scale_lo: float = 0.002,
+                      scale_hi: float = 0.01) -> dict:
+    """int8 per-output-channel weights drawn on the device: codes uniform on
+    -127..127, fp16 scales uniform on [scale_lo, scale_hi]."""
+    import torch
+    qcodes = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=device, generator=gen)
+    scales = (torch.rand((N,), device=device, generator=gen) * (scale_hi - scale_lo)
+              + scale_lo).to(torch.float16)
+    return {"N": N, "K": K, "g": 0, "qcodes": qcodes, "scales": scales}
+
+
+def activations_device(gen, T: int, K: int, device):
+    """bf16 activations ~ N(0, 1) drawn on the device."""
+    import torch
+    return torch.randn((T, K), device=device, generator=gen).to(torch.bfloat16)

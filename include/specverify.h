@@ -31,8 +31,11 @@
  * and tokens per pass": 4-bit asymmetric Medium tier, 8-bit symmetric Large
  * tier, one scale shared by every value of a group; the byte layouts are this
  * library's own):
- *   int4 codes   uint8 [N][K/2]   element k of output row n in the low nibble
- *                                 of byte k/2 when k is even, high when odd
+ *   int4 codes   uint8 [N][K/2]   row n as 4-byte groups, one per 8 consecutive
+ *                                 k: byte j (0..3) of group w holds k = 8w+j in
+ *                                 its low nibble and k = 8w+j+4 in its high
+ *                                 nibble (lets the kernel turn a byte pair into
+ *                                 a bf16 pair with one permute)
  *   int4 scales  fp16  [K/g][N]   one row per quantisation group of g
  *                                 consecutive k
  *   int4 zeros   uint8 [K/g][N/2] uint4 zero points, low nibble = even n
@@ -179,7 +182,7 @@ int spec_accept_tree(spec_ctx* ctx, const float* target_logits,
 
 /* Dequantised weights as fp32 [N][K] (exact: (code - zero) * scale and
  * code * scale both fit in fp32), for checking a packed checkpoint.  Layouts
- * and size rules as the GEMMs (int4 additionally N % 2 == 0 only). */
+ * and size rules as the GEMMs (int4 only needs N % 2 == 0 and K % 8 == 0). */
 int qdequant_w4(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
                 const uint8_t* zeros, int group_size, int N, int K, float* w,
                 void* stream);

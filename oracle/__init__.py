@@ -61,13 +61,14 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def unpack_w4_codes(qcodes: np.ndarray, N: int, K: int) -> np.ndarray:
-    """uint8 [N][K/2] -> int64 [N][K]; element k sits in the low nibble of
-    byte k//2 when k is even, in the high nibble when k is odd."""
-    q = np.asarray(qcodes, dtype=np.uint8).reshape(N, K // 2).astype(np.int64)
-    out = np.empty((N, K), dtype=np.int64)
-    out[:, 0::2] = q & 0xF
-    out[:, 1::2] = q >> 4
-    return out
+    """uint8 [N][K/2] -> int64 [N][K].  The row is read as groups of four
+    bytes, one group per eight consecutive k: byte j of a group holds the
+    group's element j in its low nibble and element j+4 in its high nibble."""
+    q = np.asarray(qcodes, dtype=np.uint8).reshape(N, K // 8, 4).astype(np.int64)
+    out = np.empty((N, K // 8, 8), dtype=np.int64)
+    out[:, :, 0:4] = q & 0xF
+    out[:, :, 4:8] = q >> 4
+    return out.reshape(N, K)
 
 
 def unpack_w4_zeros(zeros: np.ndarray, G: int, N: int) -> np.ndarray:

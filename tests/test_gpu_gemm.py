@@ -119,18 +119,19 @@ def test_w4_integer_special_case_is_exact(ctx):
     np.testing.assert_array_equal(y, exact.astype(np.float64))
 
 
-def test_deterministic_and_counters_reset(ctx):
+def test_counters_and_slots_reset_between_calls(ctx):
+    # Split tiles are summed in a shared fp32 slot that the last contributor
+    # clears; a different shape in between must not see stale sums.
     rng = np.random.default_rng(6)
     A = inputs.w4_weights(rng, 2048, 2048, 64)
     B = inputs.w4_weights(rng, 1056, 768, 64)
     xa = inputs.activations(rng, 16, 2048)
     xb = inputs.activations(rng, 32, 768)
-    ya1 = _run_w4(ctx, A, xa, 16)
-    yb = _run_w4(ctx, B, xb, 32)
-    ya2 = _run_w4(ctx, A, xa, 16)
-    np.testing.assert_array_equal(ya1, ya2)
+    refa = oracle.qgemm_w4a16(A.qcodes, A.scales, A.zeros, 64, xa, 16, 2048, 2048)
     refb = oracle.qgemm_w4a16(B.qcodes, B.scales, B.zeros, 64, xb, 32, 1056, 768)
-    assert gemm_error_ratio(yb, refb, False) <= 1.0
+    for _ in range(3):
+        assert gemm_error_ratio(_run_w4(ctx, A, xa, 16), refa, False) <= 1.0
+        assert gemm_error_ratio(_run_w4(ctx, B, xb, 32), refb, False) <= 1.0
 
 
 def test_dequant_export_bit_exact(ctx):

@@ -16,16 +16,24 @@ def _f16(vals):
 
 
 def test_w4_dequant_hand_example():
-    # N=2 rows, K=4, groups of 2 along k.
-    # row 0 codes [10, 3, 15, 0] -> bytes 0x3A, 0x0F ; row 1 codes [1, 2, 7, 8] -> 0x21, 0x87
-    qcodes = np.array([[0x3A, 0x0F], [0x21, 0x87]], dtype=np.uint8)
+    # N=2 rows, K=8, groups of 4 along k.  Byte j of each 4-byte group holds
+    # element j (low nibble) and element j+4 (high nibble).
+    # row 0 codes [10, 3, 15, 0, 1, 2, 3, 4] -> bytes 0x1A, 0x23, 0x3F, 0x40
+    # row 1 codes [1, 2, 7, 8, 9, 10, 11, 12] -> bytes 0x91, 0xA2, 0xB7, 0xC8
+    qcodes = np.array([[0x1A, 0x23, 0x3F, 0x40], [0x91, 0xA2, 0xB7, 0xC8]], dtype=np.uint8)
     # zeros [G=2][N/2=1]: group 0 -> (n0=5, n1=1) = 0x15 ; group 1 -> (n0=0, n1=9) = 0x90
     zeros = np.array([[0x15], [0x90]], dtype=np.uint8)
     scales = _f16([[0.5, 2.0], [0.25, 1.0]])   # [G][N]
-    w = oracle.dequant_w4(qcodes, scales, zeros, 2, 2, 4)
-    expected = np.array([[(10 - 5) * 0.5, (3 - 5) * 0.5, (15 - 0) * 0.25, (0 - 0) * 0.25],
-                         [(1 - 1) * 2.0, (2 - 1) * 2.0, (7 - 9) * 1.0, (8 - 9) * 1.0]])
+    w = oracle.dequant_w4(qcodes, scales, zeros, 4, 2, 8)
+    expected = np.array([[2.5, -1.0, 5.0, -2.5, 0.25, 0.5, 0.75, 1.0],
+                         [0.0, 2.0, 12.0, 14.0, 0.0, 1.0, 2.0, 3.0]])
     np.testing.assert_array_equal(w, expected)
+
+
+def test_w4_generator_packing_matches_layout():
+    codes = np.arange(16, dtype=np.uint8)[None, :] % 16   # k = 0..15
+    packed = inputs.pack_w4_codes(codes)
+    assert list(packed[0]) == [0x40, 0x51, 0x62, 0x73, 0xC8, 0xD9, 0xEA, 0xFB]
 
 
 def test_w4_zero_points_zero_scales_one_gives_codes():
@@ -59,8 +67,8 @@ def _brute_w4(qcodes, scales, zeros, g, xbits, T, N, K):
     y = [[0.0] * N for _ in range(T)]
     for n in range(N):
         for k in range(K):
-            byte = int(qcodes[n, k // 2])
-            code = (byte >> 4) if (k & 1) else (byte & 0xF)
+            byte = int(qcodes[n, (k // 8) * 4 + (k % 4)])
+            code = (byte >> 4) if (k % 8) >= 4 else (byte & 0xF)
             zb = int(zeros[k // g, n // 2])
             zero = (zb >> 4) if (n & 1) else (zb & 0xF)
             w = (code - zero) * float(scales[k // g, n])
@@ -69,7 +77,7 @@ def _brute_w4(qcodes, scales, zeros, g, xbits, T, N, K):
     return np.array(y)
 
 
-@pytest.mark.parametrize("T,N,K,g", [(3, 6, 8, 4), (2, 4, 128, 64), (1, 2, 64, 64)])
+@pytest.mark.parametrize("T,N,K,g", [(3, 6, 16, 4), (2, 4, 128, 64), (1, 2, 64, 64)])
 def test_w4_gemm_brute_force(T, N, K, g):
     rng = np.random.default_rng(10 + T + N)
     W = inputs.w4_weights(rng, N, K, g)
@@ -122,7 +130,7 @@ def test_gemm_transposed_operand_would_fail():
     # N != K/g so a transposed scale or zero layout cannot pass the brute force above;
     # here check that the layouts are not interchangeable on a non-square case.
     rng = np.random.default_rng(6)
-    W = inputs.w4_weights(rng, 6, 8, 4)
-    a = oracle.dequant_w4(W.qcodes, W.scales, W.zeros, 4, 6, 8)
-    assert a.shape == (6, 8)
-    assert not np.array_equal(a[:, :4], a[:, 4:])
+    W = inputs.w4_weights(rng, 6, 16, 4)
+    a = oracle.dequant_w4(W.qcodes, W.scales, W.zeros, 4, 6, 16)
+    assert a.shape == (6, 16)
+    assert not np.array_equal(a[:, :4], a[:, 4:8])

@@ -164,8 +164,8 @@ int check_gemm_common(const void* x, const void* y, int y_dtype, int T, int N, i
   if (K < 64 || K % 64) return set_error(SPEC_ERR_SHAPE, "K=%d not a positive multiple of 64", K);
   if (K > (1 << 20)) return set_error(SPEC_ERR_SHAPE, "K=%d above 2^20", K);
   if (w4 || group_size) {
-    if (group_size < 64 || group_size % 64 || K % group_size)
-      return set_error(SPEC_ERR_SHAPE, "group_size=%d must be a multiple of 64 dividing K=%d",
+    if (group_size < 64 || (group_size & (group_size - 1)) || K % group_size)
+      return set_error(SPEC_ERR_SHAPE, "group_size=%d must be a power of two >= 64 dividing K=%d",
                        group_size, K);
   }
   if (group_size < 0) return set_error(SPEC_ERR_SHAPE, "negative group_size");

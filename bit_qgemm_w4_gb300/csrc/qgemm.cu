@@ -50,34 +50,38 @@ constexpr int kNumA = 4;           // TMEM ring of dequantised A tiles (32 colum
 
 template <int QUANT, int TPAD>
 struct Cfg {
-  static constexpr int kCodeRowBytes = QUANT == kW4 ? 32 : 64;  // one row's codes per stage
-  static constexpr int kCodeBytes = kTileM * kCodeRowBytes;
-  static constexpr int kXBytes = TPAD * 128;                    // TPAD rows x 64 bf16
-  static constexpr int kScaleBytes = kTileM * 2;
-  static constexpr int kZeroBytes = QUANT == kW4 ? kTileM / 2 : 0;
+  // One pipeline stage streams 128 contiguous code bytes of each of the 128
+  // weight rows (full-width HBM bursts): 256 k for int4, 128 k for int8.  The
+  // MMA, the TMEM rings and the group scaling work in 64-k sub-steps.
+  static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k sub-steps per stage
+  static constexpr int kStageKK = 64 * kSub;                    // k per stage
+  static constexpr int kCodeBytes = kTileM * 128;
+  static constexpr int kXBoxBytes = TPAD * 128;                 // TPAD rows x 64 bf16
   static constexpr int kXOff = 0;
-  static constexpr int kCodeOff = kXBytes;
-  static constexpr int kScaleOff = kCodeOff + kCodeBytes;
-  static constexpr int kZeroOff = kScaleOff + kScaleBytes;
-  static constexpr int kStageBytes = (kZeroOff + 128 + 1023) / 1024 * 1024;
-  static constexpr uint32_t kTx = kXBytes + kCodeBytes + kScaleBytes + kZeroBytes;
+  static constexpr int kCodeOff = kSub * kXBoxBytes;
+  static constexpr int kScaleOff = kCodeOff + kCodeBytes;       // [SR][128] fp16
+  static constexpr int kMaxSR = kSub;                           // scale rows per stage (g = 64)
+  static constexpr int kZeroOff = kScaleOff + kMaxSR * kTileM * 2;   // [SR][64] bytes
+  static constexpr int kStageBytes = (kZeroOff + kMaxSR * 64 + 1023) / 1024 * 1024;
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kSmemBudget = 110 * 1024;
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kPCols0 = 32 * kNumA;                    // P ring starts after the A ring
   static constexpr int kNumPFit = (kTmemCols - kPCols0) / TPAD;
-  static constexpr int kNumP = kNumPFit > 8 ? 8 : kNumPFit;     // TMEM ring of stage partials
+  static constexpr int kNumP = kNumPFit > 8 ? 8 : kNumPFit;     // TMEM ring of sub-step partials
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kStages >= 2, "pipeline too shallow");
   static_assert(kNumP >= 2, "TMEM partial ring too shallow");
 };
 
 struct Params {
   int T, N, K;
   int group_size;      // 0 = per output channel
-  int ks;              // stages per tile = K / 64
+  int ks;              // stages per tile = ceil(K / stage k)
+  int sr;              // scale/zero rows per stage box
   long long total;     // tiles * ks units
+  uint32_t tx;         // TMA bytes per stage
   void* y;
   int y_f32;
   float* partials;     // split tiles: [first contributor CTA][TPAD][128] fp32, kept zeroed
@@ -96,15 +100,17 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int G) 
   return (int)c;
 }
 
-// int4: one thread dequantises one row's 64 codes (32 bytes) to bf16 pairs
-// of (code - zero) in natural k order: a[j] holds k = 2j (low half) and
-// 2j+1 (high half).  Storage: byte j of each 4-byte word w holds
-// k = 8w+j in its low nibble and k = 8w+j+4 in its high nibble.
-__device__ __forceinline__ void dequant_row_w4(uint32_t code_addr, uint32_t row, uint32_t z,
+// int4: one thread dequantises 64 codes (sub-step j of its row's 128-byte
+// stage line) to bf16 pairs of (code - zero) in natural k order: a[i] holds
+// k = 2i (low half) and 2i+1 (high half).  Storage: byte b of each 4-byte
+// word holds k = 8w+b in its low nibble and k = 8w+b+4 in its high nibble.
+// The line was written by TMA with the 128-byte swizzle: 16-byte chunk c of
+// row m sits at chunk position c ^ (m & 7).
+__device__ __forceinline__ void dequant_sub_w4(uint32_t row_addr, uint32_t m, int j, uint32_t z,
                                                uint32_t (&a)[32]) {
-  const uint32_t sw = (row >> 2) & 1u;                 // 32-byte swizzle: chunk ^= addr bit 7
-  const uint4 c0 = lds128(code_addr + ((0u ^ sw) << 4));
-  const uint4 c1 = lds128(code_addr + ((1u ^ sw) << 4));
+  const uint32_t sw = m & 7u;
+  const uint4 c0 = lds128(row_addr + (((2u * j) ^ sw) << 4));
+  const uint4 c1 = lds128(row_addr + (((2u * j + 1u) ^ sw) << 4));
   const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   const uint32_t zz = (0x4300u | z) * 0x00010001u;     // bf16x2 (128 + z, 128 + z)
   const uint32_t magic = 0x43434343u;                  // high byte of bf16 128.0
@@ -120,22 +126,23 @@ __device__ __forceinline__ void dequant_row_w4(uint32_t code_addr, uint32_t row,
   }
 }
 
-// int8: one thread converts one row's 64 codes (64 bytes) to exact bf16.
-__device__ __forceinline__ void dequant_row_w8(uint32_t code_addr, uint32_t row,
+// int8: one thread converts 64 codes (sub-step j of its row's 128-byte stage
+// line, 128-byte swizzle as above) to exact bf16.
+__device__ __forceinline__ void dequant_sub_w8(uint32_t row_addr, uint32_t m, int j,
                                                uint32_t (&a)[32]) {
-  const uint32_t sw = (row >> 1) & 3u;                 // 64-byte swizzle: chunk ^= addr bits 7-8
+  const uint32_t sw = m & 7u;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint4 v = lds128(code_addr + ((uint32_t(c) ^ sw) << 4));
+    const uint4 v = lds128(row_addr + (((uint32_t)(4 * j + c) ^ sw) << 4));
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const uint32_t u = words[w] ^ 0x80808080u;       // biased bytes code + 128
       float f[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int b = 0; b < 4; ++b) {
         // fp32 2^23 + byte, minus 2^23 + 128 = code, exactly
-        f[j] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | j)) - 8388736.0f;
+        f[b] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | b)) - 8388736.0f;
       }
       a[8 * c + 2 * w] = pack_bf16x2(f[0], f[1]);
       a[8 * c + 2 * w + 1] = pack_bf16x2(f[2], f[3]);
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
-  constexpr int S = C::kStages, NA = kNumA, NP = C::kNumP;
+  constexpr int S = C::kStages, NA = kNumA, NP = C::kNumP, SUB = C::kSub;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -170,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int G = gridDim.x;
   const long long begin = unit_begin(blockIdx.x, p.total, G);
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
+  // valid 64-k sub-steps of stage kst (the last stage of a row may be partial)
+  auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) / 64); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -212,16 +221,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (long long u = begin; u < end; ++u, ++i) {
         const int tile = (int)(u / p.ks);
         const int kst = (int)(u - (long long)tile * p.ks);
+        const int nsub = nsub_of(kst);
         const int s = i % S;
         if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
         uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kTx);
-        tma_load_2d(st + C::kXOff, &tm_x, &full[s], kst * kStageK, 0);
-        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], kst * C::kCodeRowBytes,
-                         tile * kTileM, pol_w);
-        const int g = p.group_size ? (kst * kStageK) / p.group_size : 0;
-        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], tile * kTileM, g);
-        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], tile * (kTileM / 2), g);
+        mbar_arrive_expect_tx(&full[s], p.tx - (SUB - nsub) * C::kXBoxBytes);
+        for (int j = 0; j < nsub; ++j)
+          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[s],
+                      kst * C::kStageKK + 64 * j, 0);
+        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], kst * 128, tile * kTileM, pol_w);
+        const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
+        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], tile * kTileM, g0);
+        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], tile * (kTileM / 2), g0);
       }
       if (*abort_flag) {
         // drain copies still in flight into this CTA's shared memory
@@ -235,28 +246,39 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
-      int i = 0;
-      for (long long u = begin; u < end; ++u, ++i) {
-        const int s = i % S, sa = i % NA, sp = i % NP;
+      int i = 0, r = 0;
+      bool ok = true;
+      for (long long u = begin; ok && u < end; ++u, ++i) {
+        const int kst = (int)(u % p.ks);
+        const int nsub = nsub_of(kst);
+        const int s = i % S;
         if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
-        if (!mbar_wait(&a_full[sa], (i / NA) & 1, abort_flag, p.err)) break;
-        if (!mbar_wait(&p_empty[sp], ((i / NP) & 1) ^ 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint32_t a_col = tbase + sa * 32;
-        const uint32_t d_col = tbase + C::kPCols0 + sp * TPAD;
-        const uint64_t bdesc = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
+        for (int j = 0; j < nsub; ++j, ++r) {
+          const int sa = r % NA, sp = r % NP;
+          if (!mbar_wait(&a_full[sa], (r / NA) & 1, abort_flag, p.err) ||
+              !mbar_wait(&p_empty[sp], ((r / NP) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_col = tbase + sa * 32;
+          const uint32_t d_col = tbase + C::kPCols0 + sp * TPAD;
+          const uint64_t bdesc =
+              smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff + j * C::kXBoxBytes);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
-          mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
+            mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&a_empty[sa]);
+          mma_commit(&p_full[sp]);
         }
-        mma_commit(&a_empty[sa]);
-        mma_commit(&p_full[sp]);
+        if (!ok) break;
         mma_commit(&empty[s]);
       }
-      if (*abort_flag && i > 0) {
+      if (*abort_flag && r > 0) {
         volatile int no_abort = 0;
-        const int j = i - 1;
+        const int j = r - 1;
         mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
       }
     }
@@ -265,30 +287,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     const int m = q * 32 + lane;             // weight row inside the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int i = 0;
-    for (long long u = begin; u < end; ++u, ++i) {
-      const int s = i % S, sa = i % NA;
+    int i = 0, r = 0;
+    bool ok = true;
+    for (long long u = begin; ok && u < end; ++u, ++i) {
+      const int kst = (int)(u % p.ks);
+      const int nsub = nsub_of(kst);
+      const int s = i % S;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err))) break;
       const uint8_t* st = smem + s * C::kStageBytes;
-      uint32_t a[32];
-      if constexpr (QUANT == kW4) {
-        const uint32_t zb = st[C::kZeroOff + (m >> 1)];
-        const uint32_t z = (zb >> ((m & 1) * 4)) & 0xFu;
-        dequant_row_w4(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, z, a);
-      } else {
-        dequant_row_w8(smem_u32(st + C::kCodeOff) + m * C::kCodeRowBytes, m, a);
+      const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
+      const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
+      for (int j = 0; j < nsub; ++j, ++r) {
+        const int sa = r % NA;
+        uint32_t a[32];
+        if constexpr (QUANT == kW4) {
+          const int grow = (kst * C::kStageKK + 64 * j) / p.group_size - g0;
+          const uint32_t zb = st[C::kZeroOff + grow * 64 + (m >> 1)];
+          dequant_sub_w4(row_addr, m, j, (zb >> ((m & 1) * 4)) & 0xFu, a);
+        } else {
+          dequant_sub_w8(row_addr, m, j, a);
+        }
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&a_empty[sa], ((r / NA) & 1) ^ 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st_32x32b_x32(tbase + lane_base + sa * 32, a);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[sa]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&a_empty[sa], ((i / NA) & 1) ^ 1, abort_flag, p.err)))
-        break;
-      tc_fence_after();
-      tmem_st_32x32b_x32(tbase + lane_base + sa * 32, a);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[sa]);
+      if (ok && lane == 0) mbar_arrive(&empty[s]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -308,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
     bool ok = true;
-    int i = 0;
+    int i = 0, r = 0;
     long long u = begin;
     while (ok && u < end) {
       const int tile = (int)(u / p.ks);
@@ -316,29 +348,46 @@ __global__ void __launch_bounds__(kThreads, 2)
       const long long seg_end = min(end, tile_first + p.ks);
       const bool whole_tile = (u == tile_first) && (seg_end == tile_first + p.ks);
       for (; u < seg_end; ++u, ++i) {
-        const int s = i % S, sp = i % NP;
+        const int kst = (int)(u - tile_first);
+        const int nsub = nsub_of(kst);
+        const int s = i % S;
         ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err));
         if (!ok) break;
-        const float sc = __half2float(
-            reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff)[m]);
+        float sc[SUB];
+        {
+          const __half* srow = reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff);
+          const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
+#pragma unroll
+          for (int j = 0; j < SUB; ++j) {
+            const int grow = p.group_size ? (kst * C::kStageKK + 64 * j) / p.group_size - g0 : 0;
+            sc[j] = (j < nsub) ? __half2float(srow[grow * kTileM + m]) : 0.f;
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (i / NP) & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * TPAD;
 #pragma unroll
-        for (int h = 0; h < TPAD / 16; ++h) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(d_addr + h * 16, r);
-          tmem_wait_ld();
+        for (int j = 0; j < SUB; ++j) {
+          if (j >= nsub) break;
+          const int sp = r % NP;
+          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (r / NP) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * TPAD;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            acc[h * 16 + c] = fmaf(sc, __uint_as_float(r[c]), acc[h * 16 + c]);
+          for (int h = 0; h < TPAD / 16; ++h) {
+            uint32_t rr[16];
+            tmem_ld_32x32b_x16(d_addr + h * 16, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              acc[h * 16 + c] = fmaf(sc[j], __uint_as_float(rr[c]), acc[h * 16 + c]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_empty[sp]);
+          ++r;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_empty[sp]);
+        if (!ok) break;
       }
       if (!ok) break;
 
@@ -411,21 +460,18 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   rc = encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.T,
                       (uint64_t)a.K * 2, kStageK, TPAD, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
-  if (QUANT == kW4) {
-    rc = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qcodes, (uint64_t)a.K / 2,
-                        (uint64_t)a.N, (uint64_t)a.K / 2, 32, kTileM, CU_TENSOR_MAP_SWIZZLE_32B);
-  } else {
-    rc = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qcodes, (uint64_t)a.K, (uint64_t)a.N,
-                        (uint64_t)a.K, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
-  }
+  const uint64_t row_bytes = QUANT == kW4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+  rc = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qcodes, row_bytes, (uint64_t)a.N,
+                      row_bytes, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   const uint64_t groups = a.group_size ? (uint64_t)(a.K / a.group_size) : 1;
+  const int sr = a.group_size && a.group_size < C::kStageKK ? C::kStageKK / a.group_size : 1;
   rc = encode_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)a.N, groups,
-                      (uint64_t)a.N * 2, kTileM, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                      (uint64_t)a.N * 2, kTileM, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
   if (QUANT == kW4) {
     rc = encode_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.zeros, (uint64_t)a.N / 2, groups,
-                        (uint64_t)a.N / 2, kTileM / 2, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        (uint64_t)a.N / 2, kTileM / 2, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
   } else {
     tz = ts;
@@ -436,16 +482,21 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.N = a.N;
   p.K = a.K;
   p.group_size = a.group_size;
-  p.ks = a.K / kStageK;
+  p.ks = (a.K + C::kStageKK - 1) / C::kStageKK;
+  p.sr = sr;
   const long long tiles = (a.N + kTileM - 1) / kTileM;
   p.total = tiles * p.ks;
+  p.tx = C::kSub * C::kXBoxBytes + C::kCodeBytes + sr * kTileM * 2 + (QUANT == kW4 ? sr * 64 : 0);
   p.y = a.y;
   p.y_f32 = a.y_f32;
   p.partials = ctx->partials;
   p.counters = ctx->tile_counters;
   p.err = ctx->err;
+  // persistent grid of up to two CTAs per SM with an even share of units each
   long long G = 2LL * ctx->num_sms;
   if (G > p.total) G = p.total;
+  const long long per = (p.total + G - 1) / G;
+  G = (p.total + per - 1) / per;
   if (G > ctx->max_slots) return set_error(SPEC_ERR_OOM, "workspace has too few partial slots");
 
   static std::atomic<uint32_t> attr_done{0};   // per instantiation, one bit per device

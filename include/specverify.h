@@ -101,8 +101,9 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  * x' = x, or, when signs != NULL and hadamard_block > 0, the block random
  * Hadamard rotation of x (see fwht_rotate; the weights are taken as stored
  * already rotated).
- * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size % 64 == 0 and
- * K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
+ * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size a power of two
+ * >= 64 with K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or
+ * SPEC_DTYPE_F32.
  * The (code - zero) factor is exact in bf16 and each group's partial sum is
  * scaled in fp32, so the only roundings are fp32 accumulation and the final
  * store. */
@@ -114,8 +115,9 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
 /* W8A16 verify GEMM ("How Uzu optimizes bytes and tokens per pass": Large
  * checkpoint, 8-bit symmetric quantisation, no zero point).
  *   y[t][n] = sum_k x'[t][k] * code[n][k] * scale
- * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size % 64
- * == 0).  Rotation and sizes as qgemm_w4a16, except N % 8 == 0 suffices. */
+ * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size a
+ * power of two >= 64).  Rotation and sizes as qgemm_w4a16, except N % 8 == 0
+ * suffices. */
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, const uint16_t* x, void* y, int y_dtype, int T,
                 int N, int K, const int8_t* signs, int hadamard_block,

@@ -42,19 +42,24 @@
 namespace sv {
 namespace {
 
-// warp 0: TMA producer; warp 1: TMEM owner + MMA issuer; warps 2-5: dequant
-// (one per TMEM lane quadrant); warps 6-9: epilogue (one per quadrant).
-constexpr int kThreads = 320;
-constexpr int kTmemCols = 256;     // two CTAs per SM share the 512 TMEM columns
-constexpr int kNumA = 4;           // TMEM ring of dequantised A tiles (32 columns each)
+// warp 0: TMA producer; warp 1: TMEM owner + MMA issuer; warps 2-9: dequant
+// (two per TMEM lane quadrant, each taking half of a step's k groups);
+// warps 10-13: epilogue (one per quadrant).  One CTA per SM owns all of TMEM.
+constexpr int kThreads = 448;
+constexpr int kDqWarps = 8;
+constexpr int kTmemCols = 512;
 
 template <int QUANT, int TPAD>
 struct Cfg {
   // One pipeline stage streams 128 contiguous code bytes of each of the 128
-  // weight rows (full-width HBM bursts): 256 k for int4, 128 k for int8.  The
-  // MMA, the TMEM rings and the group scaling work in 64-k sub-steps.
-  static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k sub-steps per stage
+  // weight rows (full-width HBM bursts): 256 k for int4, 128 k for int8.
+  // Within a stage, work is handed between roles in steps of kSG groups of
+  // 64 k; each 64-k group gets its own fp32 partial so its scale can be
+  // applied exactly.
+  static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k groups per stage
   static constexpr int kStageKK = 64 * kSub;                    // k per stage
+  static constexpr int kSG = (QUANT == kW4 && TPAD <= 32) ? 4 : 2;   // 64-k groups per step
+  static constexpr int kSteps = kSub / kSG;                     // steps per stage
   static constexpr int kCodeBytes = kTileM * 128;
   static constexpr int kXBoxBytes = TPAD * 128;                 // TPAD rows x 64 bf16
   static constexpr int kXOff = 0;
@@ -64,15 +69,17 @@ struct Cfg {
   static constexpr int kZeroOff = kScaleOff + kMaxSR * kTileM * 2;   // [SR][64] bytes
   static constexpr int kStageBytes = (kZeroOff + kMaxSR * 64 + 1023) / 1024 * 1024;
   static constexpr int kCtrlBytes = 1024;
-  static constexpr int kSmemBudget = 110 * 1024;
+  static constexpr int kSmemBudget = 224 * 1024;
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kPCols0 = 32 * kNumA;                    // P ring starts after the A ring
-  static constexpr int kNumPFit = (kTmemCols - kPCols0) / TPAD;
-  static constexpr int kNumP = kNumPFit > 8 ? 8 : kNumPFit;     // TMEM ring of sub-step partials
+  static constexpr int kACols = 32 * kSG;                       // one A slot: a step's groups
+  static constexpr int kPCols = TPAD * kSG;                     // one P slot: a step's partials
+  static constexpr int kNumA = 2, kNumP = 2;
+  static constexpr int kPCols0 = kNumA * kACols;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  static_assert(kStages >= 2, "pipeline too shallow");
-  static_assert(kNumP >= 2, "TMEM partial ring too shallow");
+  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kPCols0 + kNumP * kPCols <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct Params {
@@ -81,7 +88,7 @@ struct Params {
   int ks;              // stages per tile = ceil(K / stage k)
   int sr;              // scale/zero rows per stage box
   long long total;     // tiles * ks units
-  uint32_t tx;         // TMA bytes per stage
+  uint32_t tx;         // TMA bytes per full stage
   void* y;
   int y_f32;
   float* partials;     // split tiles: [first contributor CTA][TPAD][128] fp32, kept zeroed
@@ -151,12 +158,12 @@ __device__ __forceinline__ void dequant_sub_w8(uint32_t row_addr, uint32_t m, in
 }
 
 template <int QUANT, int TPAD>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
-  constexpr int S = C::kStages, NA = kNumA, NP = C::kNumP, SUB = C::kSub;
+  constexpr int S = C::kStages, NA = C::kNumA, NP = C::kNumP, SUB = C::kSub, SG = C::kSG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -177,16 +184,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int G = gridDim.x;
   const long long begin = unit_begin(blockIdx.x, p.total, G);
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
-  // valid 64-k sub-steps of stage kst (the last stage of a row may be partial)
+  // valid 64-k groups of stage kst (the last stage of a row may be partial)
   auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) / 64); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4 + 1 + 4);   // dequant warps, MMA commit, epilogue warps
+      mbar_init(&empty[s], kDqWarps + 4 + 1);   // dequant warps, epilogue warps, MMA commit
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(&a_full[s], 4);
+      mbar_init(&a_full[s], kDqWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < NP; ++s) {
@@ -226,13 +233,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], p.tx - (SUB - nsub) * C::kXBoxBytes);
-        for (int j = 0; j < nsub; ++j)
-          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[s],
-                      kst * C::kStageKK + 64 * j, 0);
         tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], kst * 128, tile * kTileM, pol_w);
         const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
         tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], tile * kTileM, g0);
         if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], tile * (kTileM / 2), g0);
+        for (int j = 0; j < nsub; ++j)
+          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[s],
+                      kst * C::kStageKK + 64 * j, 0);
       }
       if (*abort_flag) {
         // drain copies still in flight into this CTA's shared memory
@@ -253,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int nsub = nsub_of(kst);
         const int s = i % S;
         if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
-        for (int j = 0; j < nsub; ++j, ++r) {
+        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
+        for (int ls = 0; ls * SG < nsub; ++ls, ++r) {
           const int sa = r % NA, sp = r % NP;
           if (!mbar_wait(&a_full[sa], (r / NA) & 1, abort_flag, p.err) ||
               !mbar_wait(&p_empty[sp], ((r / NP) & 1) ^ 1, abort_flag, p.err)) {
@@ -261,14 +269,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           tc_fence_after();
-          const uint32_t a_col = tbase + sa * 32;
-          const uint32_t d_col = tbase + C::kPCols0 + sp * TPAD;
-          const uint64_t bdesc =
-              smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff + j * C::kXBoxBytes);
+          const int ng = min(SG, nsub - ls * SG);
+          for (int jj = 0; jj < ng; ++jj) {
+            const int jg = ls * SG + jj;   // group inside the stage
+            const uint32_t a_col = tbase + sa * C::kACols + jj * 32;
+            const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + jj * TPAD;
+            const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
-            mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
+              mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&a_empty[sa]);
           mma_commit(&p_full[sp]);
@@ -282,9 +293,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kDqWarps) {
     // ------------------------------------------------------------ dequant
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;        // which half of a step's groups
     const int m = q * 32 + lane;             // weight row inside the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int i = 0, r = 0;
@@ -297,23 +309,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint8_t* st = smem + s * C::kStageBytes;
       const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
       const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
-      for (int j = 0; j < nsub; ++j, ++r) {
+      for (int ls = 0; ls * SG < nsub; ++ls, ++r) {
         const int sa = r % NA;
-        uint32_t a[32];
-        if constexpr (QUANT == kW4) {
-          const int grow = (kst * C::kStageKK + 64 * j) / p.group_size - g0;
-          const uint32_t zb = st[C::kZeroOff + grow * 64 + (m >> 1)];
-          dequant_sub_w4(row_addr, m, j, (zb >> ((m & 1) * 4)) & 0xFu, a);
-        } else {
-          dequant_sub_w8(row_addr, m, j, a);
-        }
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&a_empty[sa], ((r / NA) & 1) ^ 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        tmem_st_32x32b_x32(tbase + lane_base + sa * 32, a);
+#pragma unroll
+        for (int h = 0; h < SG / 2; ++h) {
+          const int jj = half * (SG / 2) + h;      // group inside the step
+          const int jg = ls * SG + jj;             // group inside the stage
+          if (jg < nsub) {
+            uint32_t a[32];
+            if constexpr (QUANT == kW4) {
+              const int grow = (kst * C::kStageKK + 64 * jg) / p.group_size - g0;
+              const uint32_t zb = st[C::kZeroOff + grow * 64 + (m >> 1)];
+              dequant_sub_w4(row_addr, m, jg, (zb >> ((m & 1) * 4)) & 0xFu, a);
+            } else {
+              dequant_sub_w8(row_addr, m, jg, a);
+            }
+            tmem_st_32x32b_x32(tbase + lane_base + sa * C::kACols + jj * 32, a);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -366,21 +385,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
-        for (int j = 0; j < SUB; ++j) {
-          if (j >= nsub) break;
+        for (int ls = 0; ls < C::kSteps; ++ls) {
+          if (ls * SG >= nsub) break;
           const int sp = r % NP;
           ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (r / NP) & 1, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * TPAD;
 #pragma unroll
-          for (int h = 0; h < TPAD / 16; ++h) {
-            uint32_t rr[16];
-            tmem_ld_32x32b_x16(d_addr + h * 16, rr);
-            tmem_wait_ld();
+          for (int jj = 0; jj < SG; ++jj) {
+            const int jg = ls * SG + jj;
+            if (jg < nsub) {
+              const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
+              uint32_t rr[TPAD / 16][16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              acc[h * 16 + c] = fmaf(sc[j], __uint_as_float(rr[c]), acc[h * 16 + c]);
+              for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, rr[h]);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < TPAD / 16; ++h)
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                  acc[h * 16 + c] = fmaf(sc[jg], __uint_as_float(rr[h][c]), acc[h * 16 + c]);
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -492,8 +517,8 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.partials = ctx->partials;
   p.counters = ctx->tile_counters;
   p.err = ctx->err;
-  // persistent grid of up to two CTAs per SM with an even share of units each
-  long long G = 2LL * ctx->num_sms;
+  // persistent grid of one CTA per SM with an even share of units each
+  long long G = ctx->num_sms;
   if (G > p.total) G = p.total;
   const long long per = (p.total + G - 1) / G;
   G = (p.total + per - 1) / per;

@@ -42,11 +42,15 @@
 namespace sv {
 namespace {
 
-// warp 0: TMA producer; warp 1: TMEM owner + MMA issuer; warps 2-9: dequant
-// (two per TMEM lane quadrant, each taking half of a step's k groups);
-// warps 10-13: epilogue (one per quadrant).  One CTA per SM owns all of TMEM.
-constexpr int kThreads = 448;
+// warp 0: TMEM owner + TMA producer; warps 1-8: dequant (two per TMEM lane
+// quadrant, each taking half of a step's k groups); warps 9-12: MMA issue and
+// epilogue (one per quadrant; the warp of quadrant j issues the MMAs of k
+// group j, so four warps feed the tensor core in parallel -- a single issuing
+// thread cannot keep up with small-N MMAs).  One CTA per SM owns all of TMEM.
+constexpr int kThreads = 416;
 constexpr int kDqWarps = 8;
+constexpr int kDqWarp0 = 1;
+constexpr int kEpWarp0 = kDqWarp0 + kDqWarps;
 constexpr int kTmemCols = 512;
 
 template <int QUANT, int TPAD>
@@ -190,14 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDqWarps + 4 + 1);   // dequant warps, epilogue warps, MMA commit
+      mbar_init(&empty[s], kDqWarps + 4);   // dequant warps + one MMA commit per epilogue warp
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(&a_full[s], kDqWarps);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&a_empty[s], 4);
     }
     for (int s = 0; s < NP; ++s) {
-      mbar_init(&p_full[s], 1);
+      mbar_init(&p_full[s], 4);
       mbar_init(&p_empty[s], 4);
     }
     mbar_init(wg_bar, 4);
@@ -205,13 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *fix_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tm_x);
-    prefetch_tensormap(&tm_codes);
-    prefetch_tensormap(&tm_scales);
-    if (QUANT == kW4) prefetch_tensormap(&tm_zeros);
-  }
-  if (warp == 1) {
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&tm_x);
+      prefetch_tensormap(&tm_codes);
+      prefetch_tensormap(&tm_scales);
+      if (QUANT == kW4) prefetch_tensormap(&tm_zeros);
+    }
+    __syncwarp();
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -249,54 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
-      int i = 0, r = 0;
-      bool ok = true;
-      for (long long u = begin; ok && u < end; ++u, ++i) {
-        const int kst = (int)(u % p.ks);
-        const int nsub = nsub_of(kst);
-        const int s = i % S;
-        if (!mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err)) break;
-        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
-        for (int ls = 0; ls * SG < nsub; ++ls, ++r) {
-          const int sa = r % NA, sp = r % NP;
-          if (!mbar_wait(&a_full[sa], (r / NA) & 1, abort_flag, p.err) ||
-              !mbar_wait(&p_empty[sp], ((r / NP) & 1) ^ 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int ng = min(SG, nsub - ls * SG);
-          for (int jj = 0; jj < ng; ++jj) {
-            const int jg = ls * SG + jj;   // group inside the stage
-            const uint32_t a_col = tbase + sa * C::kACols + jj * 32;
-            const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + jj * TPAD;
-            const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
-              mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(&a_empty[sa]);
-          mma_commit(&p_full[sp]);
-        }
-        if (!ok) break;
-        mma_commit(&empty[s]);
-      }
-      if (*abort_flag && r > 0) {
-        volatile int no_abort = 0;
-        const int j = r - 1;
-        mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
-      }
-    }
-  } else if (warp < 2 + kDqWarps) {
+  } else if (warp < kEpWarp0) {
     // ------------------------------------------------------------ dequant
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;        // which half of a step's groups
+    const int half = (warp - kDqWarp0) >> 2; // which half of a step's groups
     const int m = q * 32 + lane;             // weight row inside the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int i = 0, r = 0;
@@ -342,10 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && lane == 0) mbar_arrive(&empty[s]);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    // ------------------------------------------------------------ MMA issue + epilogue
+    const int q = warp & 3;                  // TMEM lane quadrant; also the k group this warp issues
     const int m = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
     uint32_t wg_phase = 0;
     auto wg_sync = [&]() -> bool {
       __syncwarp();
@@ -358,6 +320,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     float acc[TPAD];
 #pragma unroll
     for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
+    // the step whose partials are still to be added into acc (one step of lag
+    // between issuing a step's MMAs and consuming its partials)
+    int pend_r = -1, pend_ng = 0;
+    float pend_sc[SG];
+#pragma unroll
+    for (int j = 0; j < SG; ++j) pend_sc[j] = 0.f;
+
+    auto consume = [&]() -> bool {
+      const int sp = pend_r % NP;
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (pend_r / NP) & 1, abort_flag, p.err));
+      if (!okw) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int jj = 0; jj < SG; ++jj) {
+        if (jj < pend_ng) {
+          const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
+          uint32_t rr[TPAD / 16][16];
+#pragma unroll
+          for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, rr[h]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < TPAD / 16; ++h)
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              acc[h * 16 + c] = fmaf(pend_sc[jj], __uint_as_float(rr[h][c]), acc[h * 16 + c]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_empty[sp]);
+      pend_r = -1;
+      return true;
+    };
+
     bool ok = true;
     int i = 0, r = 0;
     long long u = begin;
@@ -382,39 +378,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc[j] = (j < nsub) ? __half2float(srow[grow * kTileM + m]) : 0.f;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
 #pragma unroll
         for (int ls = 0; ls < C::kSteps; ++ls) {
           if (ls * SG >= nsub) break;
-          const int sp = r % NP;
-          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (r / NP) & 1, abort_flag, p.err));
+          const int sa = r % NA, sp = r % NP;
+          const int ng = min(SG, nsub - ls * SG);
+          ok = __all_sync(0xffffffffu, mbar_wait(&a_full[sa], (r / NA) & 1, abort_flag, p.err)) &&
+               __all_sync(0xffffffffu, mbar_wait(&p_empty[sp], ((r / NP) & 1) ^ 1, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
+          if (lane == 0) {
+            if (q < ng) {
+              const int jg = ls * SG + q;
+              const uint32_t a_col = tbase + sa * C::kACols + q * 32;
+              const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + q * TPAD;
+              const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
 #pragma unroll
-          for (int jj = 0; jj < SG; ++jj) {
-            const int jg = ls * SG + jj;
-            if (jg < nsub) {
-              const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
-              uint32_t rr[TPAD / 16][16];
-#pragma unroll
-              for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, rr[h]);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < TPAD / 16; ++h)
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                  acc[h * 16 + c] = fmaf(sc[jg], __uint_as_float(rr[h][c]), acc[h * 16 + c]);
+              for (int kk = 0; kk < 4; ++kk) {
+                // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
+                mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+              }
             }
+            mma_commit(&a_empty[sa]);
+            mma_commit(&p_full[sp]);
           }
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&p_empty[sp]);
+          if (pend_r >= 0) {
+            ok = consume();
+            if (!ok) break;
+          }
+          pend_r = r;
+          pend_ng = ng;
+#pragma unroll
+          for (int j = 0; j < SG; ++j) pend_sc[j] = sc[(ls * SG + j) < SUB ? ls * SG + j : 0];
           ++r;
         }
         if (!ok) break;
+        // the stage's shared memory may be reused once this warp's MMAs reading it are done
+        if (lane == 0) mma_commit(&empty[s]);
+        __syncwarp();
       }
       if (!ok) break;
+      if (pend_r >= 0) {
+        ok = consume();
+        if (!ok) break;
+      }
 
       // ---- segment epilogue
       const int n = tile * kTileM + m;
@@ -467,11 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
     }
+    if (*abort_flag && lane == 0 && r > 0) {
+      // wait for this warp's own MMAs before the CTA frees its tensor memory
+      volatile int no_abort = 0;
+      const int j = r - 1;
+      mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }

@@ -250,6 +250,16 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// (a0, a1) += s * (x0, x1) as one packed fp32x2 FMA.
+__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float s, float x0, float x1) {
+  uint64_t acc = (uint64_t)__float_as_uint(a0) | ((uint64_t)__float_as_uint(a1) << 32);
+  const uint64_t xs = (uint64_t)__float_as_uint(x0) | ((uint64_t)__float_as_uint(x1) << 32);
+  const uint64_t ss = (uint64_t)__float_as_uint(s) | ((uint64_t)__float_as_uint(s) << 32);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(xs), "l"(ss));
+  a0 = __uint_as_float((uint32_t)acc);
+  a1 = __uint_as_float((uint32_t)(acc >> 32));
+}
+
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

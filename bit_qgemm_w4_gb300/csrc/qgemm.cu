@@ -89,6 +89,7 @@ struct Cfg {
 struct Params {
   int T, N, K;
   int group_size;      // 0 = per output channel
+  int gshift;          // log2(group_size) (group_size is a power of two)
   int ks;              // stages per tile = ceil(K / stage k)
   int sr;              // scale/zero rows per stage box
   long long total;     // tiles * ks units
@@ -161,6 +162,34 @@ __device__ __forceinline__ void dequant_sub_w8(uint32_t row_addr, uint32_t m, in
   }
 }
 
+// Position in a ring of N slots with the parity of the current lap.
+template <int N>
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Walks a CTA's range of (tile, stage) units without per-unit division.
+struct UnitIter {
+  int tile, kst, ks;
+  __device__ __forceinline__ UnitIter(long long u, int ks_) : ks(ks_) {
+    tile = (int)(u / ks_);
+    kst = (int)(u - (long long)tile * ks_);
+  }
+  __device__ __forceinline__ void next() {
+    if (++kst == ks) {
+      kst = 0;
+      ++tile;
+    }
+  }
+};
+
 template <int QUANT, int TPAD>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
@@ -188,9 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x;
   const long long begin = unit_begin(blockIdx.x, p.total, G);
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
-  // valid 64-k groups of stage kst (the last stage of a row may be partial)
-  auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) / 64); };
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -225,30 +251,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  const long long nunits = end - begin;
+  // k groups of stage kst: the stage's first group row in its scale/zero box
+  // and the number of valid 64-k groups (the last stage of a row may be partial)
+  auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) >> 6); };
+  auto grow_of = [&](int kst, int jg) {
+    return p.group_size ? (((kst * C::kStageKK + 64 * jg) >> p.gshift) - ((kst * C::kStageKK) >> p.gshift))
+                        : 0;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      int i = 0;
-      for (long long u = begin; u < end; ++u, ++i) {
-        const int tile = (int)(u / p.ks);
-        const int kst = (int)(u - (long long)tile * p.ks);
-        const int nsub = nsub_of(kst);
-        const int s = i % S;
-        if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, abort_flag, p.err)) break;
+      UnitIter it(begin, p.ks);
+      Ring<S> st_ring;
+      long long n = 0;
+      for (; n < nunits; ++n, it.next(), st_ring.next()) {
+        const int nsub = nsub_of(it.kst);
+        const int s = st_ring.slot;
+        if (!mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err)) break;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], p.tx - (SUB - nsub) * C::kXBoxBytes);
-        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], kst * 128, tile * kTileM, pol_w);
-        const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
-        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], tile * kTileM, g0);
-        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], tile * (kTileM / 2), g0);
+        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], it.kst * 128, it.tile * kTileM, pol_w);
+        const int g0 = p.group_size ? (it.kst * C::kStageKK) >> p.gshift : 0;
+        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], it.tile * kTileM, g0);
+        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], it.tile * (kTileM / 2), g0);
         for (int j = 0; j < nsub; ++j)
           tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[s],
-                      kst * C::kStageKK + 64 * j, 0);
+                      it.kst * C::kStageKK + 64 * j, 0);
       }
       if (*abort_flag) {
         // drain copies still in flight into this CTA's shared memory
-        for (int j = (i > S ? i - S : 0); j < i; ++j) {
+        const int issued = (int)n;
+        for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
           volatile int no_abort = 0;
           mbar_wait(&full[j % S], (j / S) & 1, &no_abort, nullptr, kDrainLimitNs);
         }
@@ -260,20 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kDqWarp0) >> 2; // which half of a step's groups
     const int m = q * 32 + lane;             // weight row inside the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int i = 0, r = 0;
+    const uint32_t zshift = (m & 1) * 4;
+    UnitIter it(begin, p.ks);
+    Ring<S> st_ring;
+    Ring<NA> a_ring;
     bool ok = true;
-    for (long long u = begin; ok && u < end; ++u, ++i) {
-      const int kst = (int)(u % p.ks);
-      const int nsub = nsub_of(kst);
-      const int s = i % S;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err))) break;
+    for (long long n = 0; ok && n < nunits; ++n, it.next(), st_ring.next()) {
+      const int nsub = nsub_of(it.kst);
+      const int s = st_ring.slot;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err))) break;
       const uint8_t* st = smem + s * C::kStageBytes;
       const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
-      const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
-      for (int ls = 0; ls * SG < nsub; ++ls, ++r) {
-        const int sa = r % NA;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&a_empty[sa], ((r / NA) & 1) ^ 1, abort_flag, p.err))) {
+      for (int ls = 0; ls * SG < nsub; ++ls, a_ring.next()) {
+        const int sa = a_ring.slot;
+        if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -285,9 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jg < nsub) {
             uint32_t a[32];
             if constexpr (QUANT == kW4) {
-              const int grow = (kst * C::kStageKK + 64 * jg) / p.group_size - g0;
-              const uint32_t zb = st[C::kZeroOff + grow * 64 + (m >> 1)];
-              dequant_sub_w4(row_addr, m, jg, (zb >> ((m & 1) * 4)) & 0xFu, a);
+              const uint32_t zb = st[C::kZeroOff + grow_of(it.kst, jg) * 64 + (m >> 1)];
+              dequant_sub_w4(row_addr, m, jg, (zb >> zshift) & 0xFu, a);
             } else {
               dequant_sub_w8(row_addr, m, jg, a);
             }
@@ -322,14 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
     // the step whose partials are still to be added into acc (one step of lag
     // between issuing a step's MMAs and consuming its partials)
-    int pend_r = -1, pend_ng = 0;
+    bool pending = false;
+    int pend_slot = 0, pend_ng = 0;
+    uint32_t pend_phase = 0;
     float pend_sc[SG];
 #pragma unroll
     for (int j = 0; j < SG; ++j) pend_sc[j] = 0.f;
 
     auto consume = [&]() -> bool {
-      const int sp = pend_r % NP;
-      const bool okw = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], (pend_r / NP) & 1, abort_flag, p.err));
+      const int sp = pend_slot;
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], pend_phase, abort_flag, p.err));
       if (!okw) return false;
       tc_fence_after();
 #pragma unroll
@@ -340,52 +377,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, rr[h]);
           tmem_wait_ld();
+          const float sc = pend_sc[jj];
 #pragma unroll
           for (int h = 0; h < TPAD / 16; ++h)
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              acc[h * 16 + c] = fmaf(pend_sc[jj], __uint_as_float(rr[h][c]), acc[h * 16 + c]);
+            for (int c = 0; c < 16; c += 2)
+              fma_f32x2(acc[h * 16 + c], acc[h * 16 + c + 1], sc, __uint_as_float(rr[h][c]),
+                        __uint_as_float(rr[h][c + 1]));
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_empty[sp]);
-      pend_r = -1;
+      pending = false;
       return true;
     };
 
     bool ok = true;
-    int i = 0, r = 0;
-    long long u = begin;
-    while (ok && u < end) {
-      const int tile = (int)(u / p.ks);
+    UnitIter it(begin, p.ks);
+    Ring<S> st_ring;
+    Ring<NA> a_ring;
+    Ring<NP> p_ring;
+    long long n = 0;
+    while (ok && n < nunits) {
+      const int tile = it.tile;
       const long long tile_first = (long long)tile * p.ks;
+      const long long u0 = begin + n;
       const long long seg_end = min(end, tile_first + p.ks);
-      const bool whole_tile = (u == tile_first) && (seg_end == tile_first + p.ks);
-      for (; u < seg_end; ++u, ++i) {
-        const int kst = (int)(u - tile_first);
+      const bool whole_tile = (u0 == tile_first) && (seg_end == tile_first + p.ks);
+      for (long long u = u0; u < seg_end; ++u, ++n, it.next(), st_ring.next()) {
+        const int kst = it.kst;
         const int nsub = nsub_of(kst);
-        const int s = i % S;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / S) & 1, abort_flag, p.err));
+        const int s = st_ring.slot;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err));
         if (!ok) break;
         float sc[SUB];
         {
           const __half* srow = reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff);
-          const int g0 = p.group_size ? (kst * C::kStageKK) / p.group_size : 0;
 #pragma unroll
-          for (int j = 0; j < SUB; ++j) {
-            const int grow = p.group_size ? (kst * C::kStageKK + 64 * j) / p.group_size - g0 : 0;
-            sc[j] = (j < nsub) ? __half2float(srow[grow * kTileM + m]) : 0.f;
-          }
+          for (int j = 0; j < SUB; ++j)
+            sc[j] = (j < nsub) ? __half2float(srow[grow_of(kst, j) * kTileM + m]) : 0.f;
         }
         const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
 #pragma unroll
         for (int ls = 0; ls < C::kSteps; ++ls) {
           if (ls * SG >= nsub) break;
-          const int sa = r % NA, sp = r % NP;
+          const int sa = a_ring.slot, sp = p_ring.slot;
           const int ng = min(SG, nsub - ls * SG);
-          ok = __all_sync(0xffffffffu, mbar_wait(&a_full[sa], (r / NA) & 1, abort_flag, p.err)) &&
-               __all_sync(0xffffffffu, mbar_wait(&p_empty[sp], ((r / NP) & 1) ^ 1, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err)) &&
+               __all_sync(0xffffffffu, mbar_wait(&p_empty[sp], p_ring.phase ^ 1, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
@@ -404,15 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&p_full[sp]);
           }
           __syncwarp();
-          if (pend_r >= 0) {
+          if (pending) {
             ok = consume();
             if (!ok) break;
           }
-          pend_r = r;
+          pending = true;
+          pend_slot = sp;
+          pend_phase = p_ring.phase;
           pend_ng = ng;
 #pragma unroll
           for (int j = 0; j < SG; ++j) pend_sc[j] = sc[(ls * SG + j) < SUB ? ls * SG + j : 0];
-          ++r;
+          a_ring.next();
+          p_ring.next();
         }
         if (!ok) break;
         // the stage's shared memory may be reused once this warp's MMAs reading it are done
@@ -420,13 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (pend_r >= 0) {
+      if (pending) {
         ok = consume();
         if (!ok) break;
       }
 
       // ---- segment epilogue
-      const int n = tile * kTileM + m;
+      const int nrow = tile * kTileM + m;
       bool store = whole_tile;
       if (!whole_tile) {
         // Split tile: add this CTA's partial into the tile's fp32 slot (keyed
@@ -460,27 +503,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wg_sync();
         if (!ok) break;
       }
-      if (store && n < p.N) {
+      if (store && nrow < p.N) {
         if (p.y_f32) {
           float* y = reinterpret_cast<float*>(p.y);
 #pragma unroll
           for (int t = 0; t < TPAD; ++t)
-            if (t < p.T) y[(size_t)t * p.N + n] = acc[t];
+            if (t < p.T) y[(size_t)t * p.N + nrow] = acc[t];
         } else {
           __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
 #pragma unroll
           for (int t = 0; t < TPAD; ++t)
-            if (t < p.T) y[(size_t)t * p.N + n] = __float2bfloat16_rn(acc[t]);
+            if (t < p.T) y[(size_t)t * p.N + nrow] = __float2bfloat16_rn(acc[t]);
         }
       }
 #pragma unroll
       for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
     }
-    if (*abort_flag && lane == 0 && r > 0) {
+    if (*abort_flag && lane == 0 && pending) {
       // wait for this warp's own MMAs before the CTA frees its tensor memory
       volatile int no_abort = 0;
-      const int j = r - 1;
-      mbar_wait(&p_full[j % NP], (j / NP) & 1, &no_abort, nullptr, kDrainLimitNs);
+      mbar_wait(&p_full[pend_slot], pend_phase, &no_abort, nullptr, kDrainLimitNs);
     }
   }
 
@@ -522,6 +564,8 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.N = a.N;
   p.K = a.K;
   p.group_size = a.group_size;
+  p.gshift = 0;
+  while (a.group_size && (1 << p.gshift) < a.group_size) ++p.gshift;
   p.ks = (a.K + C::kStageKK - 1) / C::kStageKK;
   p.sr = sr;
   const long long tiles = (a.N + kTileM - 1) / kTileM;

@@ -42,15 +42,12 @@
 namespace sv {
 namespace {
 
-// warp 0: TMEM owner + TMA producer; warps 1-8: dequant (two per TMEM lane
-// quadrant, each taking half of a step's k groups); warps 9-12: MMA issue and
-// epilogue (one per quadrant; the warp of quadrant j issues the MMAs of k
-// group j, so four warps feed the tensor core in parallel -- a single issuing
-// thread cannot keep up with small-N MMAs).  One CTA per SM owns all of TMEM.
-constexpr int kThreads = 416;
-constexpr int kDqWarps = 8;
-constexpr int kDqWarp0 = 1;
-constexpr int kEpWarp0 = kDqWarp0 + kDqWarps;
+// Roles: warp 0 owns TMEM and streams stages with TMA; then 4*kSG dequant
+// warps (one per TMEM lane quadrant and k group of a step); then kSG MMA
+// warps (warp j issues the MMAs of k group j -- several issuing warps keep
+// the tensor core fed, a single one cannot with small-N MMAs); then four
+// epilogue warps (one per quadrant) that fold the group partials into fp32
+// accumulators and write the output.  One CTA per SM owns all of TMEM.
 constexpr int kTmemCols = 512;
 
 template <int QUANT, int TPAD>
@@ -81,6 +78,11 @@ struct Cfg {
   static constexpr int kNumA = 2, kNumP = 2;
   static constexpr int kPCols0 = kNumA * kACols;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
+  static constexpr int kDqWarps = 4 * kSG;
+  static constexpr int kDqWarp0 = 1;
+  static constexpr int kMmaWarp0 = kDqWarp0 + kDqWarps;
+  static constexpr int kEpWarp0 = kMmaWarp0 + kSG;
+  static constexpr int kThreads = 32 * (kEpWarp0 + 4);
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kPCols0 + kNumP * kPCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -191,7 +193,7 @@ struct UnitIter {
 };
 
 template <int QUANT, int TPAD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
@@ -217,17 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x;
   const long long begin = unit_begin(blockIdx.x, p.total, G);
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDqWarps + 4);   // dequant warps + one MMA commit per epilogue warp
+      mbar_init(&empty[s], C::kDqWarps + SG + 4);   // dequant warps, MMA commits, epilogue warps
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(&a_full[s], kDqWarps);
-      mbar_init(&a_empty[s], 4);
+      mbar_init(&a_full[s], C::kDqWarps);
+      mbar_init(&a_empty[s], SG);
     }
     for (int s = 0; s < NP; ++s) {
-      mbar_init(&p_full[s], 4);
+      mbar_init(&p_full[s], SG);
       mbar_init(&p_empty[s], 4);
     }
     mbar_init(wg_bar, 4);
@@ -252,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const long long nunits = end - begin;
-  // k groups of stage kst: the stage's first group row in its scale/zero box
-  // and the number of valid 64-k groups (the last stage of a row may be partial)
+  // valid 64-k groups of stage kst (the last stage of a row may be partial)
+  // and the scale/zero row of group jg inside the stage's box
   auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) >> 6); };
   auto grow_of = [&](int kst, int jg) {
     return p.group_size ? (((kst * C::kStageKK + 64 * jg) >> p.gshift) - ((kst * C::kStageKK) >> p.gshift))
@@ -290,12 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < kEpWarp0) {
+  } else if (warp < C::kMmaWarp0) {
     // ------------------------------------------------------------ dequant
-    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int half = (warp - kDqWarp0) >> 2; // which half of a step's groups
-    const int m = q * 32 + lane;             // weight row inside the tile
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+    const int jj = (warp - C::kDqWarp0) >> 2;     // k group of each step this warp handles
+    const int m = q * 32 + lane;                  // weight row inside the tile
+    const uint32_t a_addr0 = tbase + ((uint32_t)(q * 32) << 16) + jj * 32;
     const uint32_t zshift = (m & 1) * 4;
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
@@ -308,41 +311,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* st = smem + s * C::kStageBytes;
       const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
       for (int ls = 0; ls * SG < nsub; ++ls, a_ring.next()) {
+        const int jg = ls * SG + jj;              // group inside the stage
+        uint32_t a[32];
+        if (jg < nsub) {
+          if constexpr (QUANT == kW4) {
+            const uint32_t zb = st[C::kZeroOff + grow_of(it.kst, jg) * 64 + (m >> 1)];
+            dequant_sub_w4(row_addr, m, jg, (zb >> zshift) & 0xFu, a);
+          } else {
+            dequant_sub_w8(row_addr, m, jg, a);
+          }
+        }
         const int sa = a_ring.slot;
         if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < SG / 2; ++h) {
-          const int jj = half * (SG / 2) + h;      // group inside the step
-          const int jg = ls * SG + jj;             // group inside the stage
-          if (jg < nsub) {
-            uint32_t a[32];
-            if constexpr (QUANT == kW4) {
-              const uint32_t zb = st[C::kZeroOff + grow_of(it.kst, jg) * 64 + (m >> 1)];
-              dequant_sub_w4(row_addr, m, jg, (zb >> zshift) & 0xFu, a);
-            } else {
-              dequant_sub_w8(row_addr, m, jg, a);
-            }
-            tmem_st_32x32b_x32(tbase + lane_base + sa * C::kACols + jj * 32, a);
-          }
+        if (jg < nsub) {
+          tc_fence_after();
+          tmem_st_32x32b_x32(a_addr0 + sa * C::kACols, a);
+          tmem_wait_st();
+          tc_fence_before();
         }
-        tmem_wait_st();
-        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[sa]);
       }
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(&empty[s]);
     }
+  } else if (warp < C::kEpWarp0) {
+    // ------------------------------------------------------------ MMA issue (k group jj)
+    if (lane == 0) {
+      const int jj = warp - C::kMmaWarp0;
+      constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
+      UnitIter it(begin, p.ks);
+      Ring<S> st_ring;
+      Ring<NA> a_ring;
+      Ring<NP> p_ring;
+      bool ok = true, issued_any = false;
+      int last_sp = 0;
+      uint32_t last_phase = 0;
+      for (long long n = 0; ok && n < nunits; ++n, it.next(), st_ring.next()) {
+        const int nsub = nsub_of(it.kst);
+        const int s = st_ring.slot;
+        if (!mbar_wait(&full[s], st_ring.phase, abort_flag, p.err)) break;
+        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
+        for (int ls = 0; ls * SG < nsub; ++ls, a_ring.next(), p_ring.next()) {
+          const int sa = a_ring.slot, sp = p_ring.slot;
+          if (!mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err) ||
+              !mbar_wait(&p_empty[sp], p_ring.phase ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int jg = ls * SG + jj;
+          if (jg < nsub) {
+            const uint32_t a_col = tbase + sa * C::kACols + jj * 32;
+            const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + jj * TPAD;
+            const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
+              mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&a_empty[sa]);
+          mma_commit(&p_full[sp]);
+          issued_any = true;
+          last_sp = sp;
+          last_phase = p_ring.phase;
+        }
+        if (!ok) break;
+        // the stage's shared memory may be reused once these MMAs are done
+        mma_commit(&empty[s]);
+      }
+      if (*abort_flag && issued_any) {
+        // wait for this thread's own MMAs before the CTA frees its tensor memory
+        volatile int no_abort = 0;
+        mbar_wait(&p_full[last_sp], last_phase, &no_abort, nullptr, kDrainLimitNs);
+      }
+    }
   } else {
-    // ------------------------------------------------------------ MMA issue + epilogue
-    const int q = warp & 3;                  // TMEM lane quadrant; also the k group this warp issues
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
     uint32_t wg_phase = 0;
     auto wg_sync = [&]() -> bool {
       __syncwarp();
@@ -355,48 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float acc[TPAD];
 #pragma unroll
     for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-    // the step whose partials are still to be added into acc (one step of lag
-    // between issuing a step's MMAs and consuming its partials)
-    bool pending = false;
-    int pend_slot = 0, pend_ng = 0;
-    uint32_t pend_phase = 0;
-    float pend_sc[SG];
-#pragma unroll
-    for (int j = 0; j < SG; ++j) pend_sc[j] = 0.f;
-
-    auto consume = [&]() -> bool {
-      const int sp = pend_slot;
-      const bool okw = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], pend_phase, abort_flag, p.err));
-      if (!okw) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int jj = 0; jj < SG; ++jj) {
-        if (jj < pend_ng) {
-          const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
-          uint32_t rr[TPAD / 16][16];
-#pragma unroll
-          for (int h = 0; h < TPAD / 16; ++h) tmem_ld_32x32b_x16(d_addr + h * 16, rr[h]);
-          tmem_wait_ld();
-          const float sc = pend_sc[jj];
-#pragma unroll
-          for (int h = 0; h < TPAD / 16; ++h)
-#pragma unroll
-            for (int c = 0; c < 16; c += 2)
-              fma_f32x2(acc[h * 16 + c], acc[h * 16 + c + 1], sc, __uint_as_float(rr[h][c]),
-                        __uint_as_float(rr[h][c + 1]));
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_empty[sp]);
-      pending = false;
-      return true;
-    };
-
     bool ok = true;
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
-    Ring<NA> a_ring;
     Ring<NP> p_ring;
     long long n = 0;
     while (ok && n < nunits) {
@@ -418,55 +431,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < SUB; ++j)
             sc[j] = (j < nsub) ? __half2float(srow[grow_of(kst, j) * kTileM + m]) : 0.f;
         }
-        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
         for (int ls = 0; ls < C::kSteps; ++ls) {
           if (ls * SG >= nsub) break;
-          const int sa = a_ring.slot, sp = p_ring.slot;
-          const int ng = min(SG, nsub - ls * SG);
-          ok = __all_sync(0xffffffffu, mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err)) &&
-               __all_sync(0xffffffffu, mbar_wait(&p_empty[sp], p_ring.phase ^ 1, abort_flag, p.err));
+          const int sp = p_ring.slot;
+          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], p_ring.phase, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            if (q < ng) {
-              const int jg = ls * SG + q;
-              const uint32_t a_col = tbase + sa * C::kACols + q * 32;
-              const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + q * TPAD;
-              const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
-                mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+          for (int jj = 0; jj < SG; ++jj) {
+            const int jg = ls * SG + jj;
+            if (jg < nsub) {
+              const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
+              const float scj = sc[jg < SUB ? jg : 0];
+#pragma unroll
+              for (int h = 0; h < TPAD / 16; ++h) {
+                uint32_t rr[16];
+                tmem_ld_32x32b_x16(d_addr + h * 16, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; c += 2)
+                  fma_f32x2(acc[h * 16 + c], acc[h * 16 + c + 1], scj, __uint_as_float(rr[c]),
+                            __uint_as_float(rr[c + 1]));
               }
             }
-            mma_commit(&a_empty[sa]);
-            mma_commit(&p_full[sp]);
           }
+          tc_fence_before();
           __syncwarp();
-          if (pending) {
-            ok = consume();
-            if (!ok) break;
-          }
-          pending = true;
-          pend_slot = sp;
-          pend_phase = p_ring.phase;
-          pend_ng = ng;
-#pragma unroll
-          for (int j = 0; j < SG; ++j) pend_sc[j] = sc[(ls * SG + j) < SUB ? ls * SG + j : 0];
-          a_ring.next();
+          if (lane == 0) mbar_arrive(&p_empty[sp]);
           p_ring.next();
         }
         if (!ok) break;
-        // the stage's shared memory may be reused once this warp's MMAs reading it are done
-        if (lane == 0) mma_commit(&empty[s]);
-        __syncwarp();
       }
       if (!ok) break;
-      if (pending) {
-        ok = consume();
-        if (!ok) break;
-      }
 
       // ---- segment epilogue
       const int nrow = tile * kTileM + m;
@@ -518,11 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-    }
-    if (*abort_flag && lane == 0 && pending) {
-      // wait for this warp's own MMAs before the CTA frees its tensor memory
-      volatile int no_abort = 0;
-      mbar_wait(&p_full[pend_slot], pend_phase, &no_abort, nullptr, kDrainLimitNs);
     }
   }
 
@@ -593,7 +587,7 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
     if (rc) return rc;
     attr_done.fetch_or(bit);
   }
-  qgemm_kernel<QUANT, TPAD><<<(unsigned)G, kThreads, C::kSmemBytes, stream>>>(tx, tc, ts, tz, p);
+  qgemm_kernel<QUANT, TPAD><<<(unsigned)G, C::kThreads, C::kSmemBytes, stream>>>(tx, tc, ts, tz, p);
   return check_cuda(cudaGetLastError(), "qgemm launch");
 }
 

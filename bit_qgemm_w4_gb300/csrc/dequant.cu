@@ -19,9 +19,10 @@ __global__ void dequant_w4_kernel(const uint8_t* __restrict__ qc, const uint16_t
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int n = (int)(i / K), k = (int)(i % K);
-    // byte j of each 4-byte group holds k = 8w+j (low nibble) and 8w+j+4 (high)
-    const uint32_t b = qc[(long long)n * (K / 2) + (k / 8) * 4 + (k % 4)];
-    const int code = (k % 8) >= 4 ? (int)(b >> 4) : (int)(b & 15u);
+    // nibble p of each 32-bit word holds k = 8w + 2*(p % 4) + p / 4
+    const int r = k & 7, pos = 4 * (r & 1) + (r >> 1);
+    const uint32_t b = qc[(long long)n * (K / 2) + (k / 8) * 4 + (pos >> 1)];
+    const int code = (pos & 1) ? (int)(b >> 4) : (int)(b & 15u);
     const int gi = k / g;
     const uint32_t zb = zr[(long long)gi * (N / 2) + n / 2];
     const int z = (n & 1) ? (int)(zb >> 4) : (int)(zb & 15u);

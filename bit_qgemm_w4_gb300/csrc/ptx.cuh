@@ -11,6 +11,7 @@ namespace sv {
 
 // Device-side error codes written into the context's error word.
 constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrRange = 4;   // an activation did not fit the GEMM's fp16 operand range
 
 // A bounded wait gives up after this long (globaltimer nanoseconds) and
 // records kDevErrTimeout.  Legitimate waits inside one launch take
@@ -225,6 +226,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);      // M / 16
 }
 
+// Same for fp16 A and B operands.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4)                          // D format: f32
+         | ((uint32_t)(n >> 3) << 17)       // N / 8  (A, B format 0 = f16)
+         | ((uint32_t)(m >> 4) << 24);      // M / 16
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
@@ -264,6 +272,34 @@ __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -5,29 +5,32 @@
 // Tooling", section "How Uzu optimizes bytes and tokens per pass": 4-bit
 // asymmetric Medium tier, 8-bit symmetric Large tier, one scale per group):
 //   y[t][n] = sum_k x[t][k] * (code[n][k] - zero[g][n]) * scale[g][n]   (int4)
-//   y[t][n] = sum_k x[t][k] *  code[n][k]              * scale[g][n]   (int8)
+//   y[t][n] = sum_k x[t][k] *  code[n][k]              * scale         (int8)
 //
-// Design (swap-AB, weight rows are the MMA's M dimension, the T drafted
-// positions its N dimension):
-//  * one pipeline stage = 128 weight rows x 64 k.  A TMA warp streams the
-//    packed codes (swizzled so that each row's bytes are bank-conflict free),
-//    the group's scales/zeros and the 64-wide activation slice into a ring of
-//    shared-memory stages;
-//  * four dequantisation warps (one per TMEM lane quadrant, one weight row per
-//    thread) turn a row's 64 codes into exact bf16 integers (code - zero, or
-//    the int8 code) and write them straight into tensor memory with
-//    tcgen05.st -- the MMA's A operand lives in TMEM, so the dequantised tile
-//    never touches shared memory;
-//  * one thread issues tcgen05.mma (A from TMEM, B = activations from shared
-//    memory, D = fp32 in TMEM), 4 x K16 per stage, into a per-stage partial
-//    accumulator;
-//  * the same dequantisation warps read each stage's partial back
-//    (tcgen05.ld) and add scale * partial into fp32 registers, so group scales
-//    are applied exactly in fp32 (no bf16 rounding of the weights at all);
-//  * work is split stream-K style: the (tile, stage) units of the whole GEMM
-//    are divided evenly over a persistent grid of two CTAs per SM; a tile cut
-//    between CTAs is finished by the last CTA to arrive (deterministic sum of
-//    per-CTA fp32 partials in CTA order, no spin-waiting on other CTAs).
+// Design (swap-AB: 128 weight rows are the MMA's M dimension, the T drafted
+// positions its N dimension; one CTA per SM owns all 512 TMEM columns):
+//  * a TMA warp streams stages into a shared-memory ring: per stage the
+//    128-byte line of codes of each of the 128 weight rows (256 k of int4 or
+//    128 k of int8 -- full-width HBM bursts), the stage's scale and zero
+//    rows, and the stage's activation boxes (bf16);
+//  * dequantisation warps, one per (TMEM lane quadrant, 64-k group), turn a
+//    row's 64 codes into fp16 weights, (code - zero) * scale rounded once
+//    (relative error <= 2^-11), and write them straight into a TMEM ring
+//    with tcgen05.st -- the MMA's A operand lives in TMEM, so dequantised
+//    weights never touch shared memory.  The same warps convert the stage's
+//    activations to fp16 in place (exact inside the fp16 range; a value
+//    outside it records an error);
+//  * two MMA warps (each issuing half of a stage's 64-k groups; several
+//    issuing warps are needed to keep the tensor core fed with small-N MMAs)
+//    accumulate D += A * B in fp32 across the whole tile segment, each into
+//    its own double-buffered TMEM accumulator;
+//  * four epilogue warps sum the two accumulators at the end of a segment
+//    (times the per-channel scale for int8 without groups, which stays exact
+//    in fp32), clear them and write the output;
+//  * work is split stream-K style: the (tile, stage) units of the GEMM are
+//    divided evenly over the persistent grid; a tile cut between CTAs is
+//    summed with red.global.add into an fp32 slot and finished by the last
+//    contributor to arrive (no CTA ever waits for another).
 // Every wait is bounded (see ptx.cuh); a timeout records an error, drains the
 // CTA's in-flight copies/MMAs and frees its tensor memory before returning.
 
@@ -42,27 +45,15 @@
 namespace sv {
 namespace {
 
-// Roles: warp 0 owns TMEM and streams stages with TMA; then 4*kSG dequant
-// warps (one per TMEM lane quadrant and k group of a step); then kSG MMA
-// warps (warp j issues the MMAs of k group j -- several issuing warps keep
-// the tensor core fed, a single one cannot with small-N MMAs); then four
-// epilogue warps (one per quadrant) that fold the group partials into fp32
-// accumulators and write the output.  One CTA per SM owns all of TMEM.
 constexpr int kTmemCols = 512;
+constexpr int kMmaWarps = 2;
 
 template <int QUANT, int TPAD>
 struct Cfg {
-  // One pipeline stage streams 128 contiguous code bytes of each of the 128
-  // weight rows (full-width HBM bursts): 256 k for int4, 128 k for int8.
-  // Within a stage, work is handed between roles in steps of kSG groups of
-  // 64 k; each 64-k group gets its own fp32 partial so its scale can be
-  // applied exactly.
   static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k groups per stage
   static constexpr int kStageKK = 64 * kSub;                    // k per stage
-  static constexpr int kSG = (QUANT == kW4 && TPAD <= 32) ? 4 : 2;   // 64-k groups per step
-  static constexpr int kSteps = kSub / kSG;                     // steps per stage
-  static constexpr int kCodeBytes = kTileM * 128;
-  static constexpr int kXBoxBytes = TPAD * 128;                 // TPAD rows x 64 bf16
+  static constexpr int kCodeBytes = kTileM * 128;               // 128 code bytes per row
+  static constexpr int kXBoxBytes = TPAD * 128;                 // TPAD rows x 64 activations
   static constexpr int kXOff = 0;
   static constexpr int kCodeOff = kSub * kXBoxBytes;
   static constexpr int kScaleOff = kCodeOff + kCodeBytes;       // [SR][128] fp16
@@ -73,19 +64,28 @@ struct Cfg {
   static constexpr int kSmemBudget = 224 * 1024;
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kACols = 32 * kSG;                       // one A slot: a step's groups
-  static constexpr int kPCols = TPAD * kSG;                     // one P slot: a step's partials
-  static constexpr int kNumA = 2, kNumP = 2;
-  static constexpr int kPCols0 = kNumA * kACols;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  static constexpr int kDqWarps = 4 * kSG;
+  // TMEM: a ring of A slots (one stage each, 32 columns per 64-k group) and
+  // two accumulator buffers, each holding one TPAD-column D per MMA warp.
+  static constexpr int kACols = 32 * kSub;
+  static constexpr int kDCols = TPAD * kMmaWarps;
+  static constexpr int kNumAFit = (kTmemCols - 2 * kDCols) / kACols;
+  static constexpr int kNumA = kNumAFit > 4 ? 4 : kNumAFit;
+  static constexpr int kD0 = kNumA * kACols;
+  static constexpr int kGroupsPerMma = kSub / kMmaWarps;
+  // warps
+  static constexpr int kDqWarps = 4 * kSub;
   static constexpr int kDqWarp0 = 1;
   static constexpr int kMmaWarp0 = kDqWarp0 + kDqWarps;
-  static constexpr int kEpWarp0 = kMmaWarp0 + kSG;
+  static constexpr int kEpWarp0 = kMmaWarp0 + kMmaWarps;
   static constexpr int kThreads = 32 * (kEpWarp0 + 4);
+  // activation chunks (16 bytes) each dequant lane converts per stage
+  static constexpr int kXChunksPerLane = (kSub * kXBoxBytes / 16) / (kDqWarps * 32);
   static_assert(kStages >= 3, "pipeline too shallow");
-  static_assert(kPCols0 + kNumP * kPCols <= kTmemCols, "TMEM budget");
+  static_assert(kNumA >= 2, "TMEM A ring too shallow");
+  static_assert(kD0 + 2 * kDCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kXChunksPerLane * kDqWarps * 32 * 16 == kSub * kXBoxBytes, "activation split");
 };
 
 struct Params {
@@ -93,9 +93,9 @@ struct Params {
   int group_size;      // 0 = per output channel
   int gshift;          // log2(group_size) (group_size is a power of two)
   int ks;              // stages per tile = ceil(K / stage k)
-  int sr;              // scale/zero rows per stage box
   long long total;     // tiles * ks units
   uint32_t tx;         // TMA bytes per full stage
+  const uint16_t* scales;   // per-channel int8 scales (epilogue)
   void* y;
   int y_f32;
   float* partials;     // split tiles: [first contributor CTA][TPAD][128] fp32, kept zeroed
@@ -112,56 +112,6 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int G) 
   while (c + 1 < G && unit_begin((int)c + 1, total, G) <= u) ++c;
   while (c > 0 && unit_begin((int)c, total, G) > u) --c;
   return (int)c;
-}
-
-// int4: one thread dequantises 64 codes (sub-step j of its row's 128-byte
-// stage line) to bf16 pairs of (code - zero) in natural k order: a[i] holds
-// k = 2i (low half) and 2i+1 (high half).  Storage: byte b of each 4-byte
-// word holds k = 8w+b in its low nibble and k = 8w+b+4 in its high nibble.
-// The line was written by TMA with the 128-byte swizzle: 16-byte chunk c of
-// row m sits at chunk position c ^ (m & 7).
-__device__ __forceinline__ void dequant_sub_w4(uint32_t row_addr, uint32_t m, int j, uint32_t z,
-                                               uint32_t (&a)[32]) {
-  const uint32_t sw = m & 7u;
-  const uint4 c0 = lds128(row_addr + (((2u * j) ^ sw) << 4));
-  const uint4 c1 = lds128(row_addr + (((2u * j + 1u) ^ sw) << 4));
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const uint32_t zz = (0x4300u | z) * 0x00010001u;     // bf16x2 (128 + z, 128 + z)
-  const uint32_t magic = 0x43434343u;                  // high byte of bf16 128.0
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t lo = words[w] & 0x0F0F0F0Fu;         // bytes: k0 k1 k2 k3
-    const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;  // bytes: k4 k5 k6 k7
-    // bf16x2 (128 + c_a, 128 + c_b) = bytes {c_a, 0x43, c_b, 0x43}
-    a[4 * w + 0] = sub_bf16x2(__byte_perm(lo, magic, 0x4140u), zz);
-    a[4 * w + 1] = sub_bf16x2(__byte_perm(lo, magic, 0x4342u), zz);
-    a[4 * w + 2] = sub_bf16x2(__byte_perm(hi, magic, 0x4140u), zz);
-    a[4 * w + 3] = sub_bf16x2(__byte_perm(hi, magic, 0x4342u), zz);
-  }
-}
-
-// int8: one thread converts 64 codes (sub-step j of its row's 128-byte stage
-// line, 128-byte swizzle as above) to exact bf16.
-__device__ __forceinline__ void dequant_sub_w8(uint32_t row_addr, uint32_t m, int j,
-                                               uint32_t (&a)[32]) {
-  const uint32_t sw = m & 7u;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 v = lds128(row_addr + (((uint32_t)(4 * j + c) ^ sw) << 4));
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint32_t u = words[w] ^ 0x80808080u;       // biased bytes code + 128
-      float f[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        // fp32 2^23 + byte, minus 2^23 + 128 = code, exactly
-        f[b] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | b)) - 8388736.0f;
-      }
-      a[8 * c + 2 * w] = pack_bf16x2(f[0], f[1]);
-      a[8 * c + 2 * w + 1] = pack_bf16x2(f[2], f[3]);
-    }
-  }
 }
 
 // Position in a ring of N slots with the parity of the current lap.
@@ -192,13 +142,69 @@ struct UnitIter {
   }
 };
 
+// int4: 64 codes (group j of the row's 128-byte stage line) to fp16 weights
+// (code - zero) * scale in natural k order: a[i] holds k = 2i (low half) and
+// 2i+1 (high half).  Code layout: nibble p (0..7, from the least significant
+// end) of each little-endian 32-bit word holds k = 8w + 2*(p % 4) + p / 4, so
+// masking nibbles {0, 4} gives the pair (k0, k1), {1, 5} gives (k2, k3), and
+// the same on the word shifted by 8 gives (k4, k5), (k6, k7).  A nibble in
+// bits 0-3 of a half becomes 1024 + c with the fp16 exponent of 1024, a
+// nibble in bits 4-7 becomes 64 + c with the exponent of 64 -- both exact.
+// The line was written by TMA with the 128-byte swizzle: 16-byte chunk c of
+// row m sits at chunk position c ^ (m & 7).
+__device__ __forceinline__ void dequant_w4(uint32_t row_addr, uint32_t m, int j, uint32_t z,
+                                           uint32_t s2, uint32_t (&a)[32]) {
+  const uint32_t sw = m & 7u;
+  const uint4 c0 = lds128(row_addr + (((2u * j) ^ sw) << 4));
+  const uint4 c1 = lds128(row_addr + (((2u * j + 1u) ^ sw) << 4));
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t zlo = (0x6400u | z) * 0x00010001u;            // fp16x2 (1024 + z)
+  const uint32_t zhi = (0x5400u | (z << 4)) * 0x00010001u;     // fp16x2 (64 + z)
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t q = words[w];
+    const uint32_t q8 = q >> 8;
+    a[4 * w + 0] = mul_f16x2(sub_f16x2(lop3_and_or(q, 0x000F000Fu, 0x64006400u), zlo), s2);
+    a[4 * w + 1] = mul_f16x2(sub_f16x2(lop3_and_or(q, 0x00F000F0u, 0x54005400u), zhi), s2);
+    a[4 * w + 2] = mul_f16x2(sub_f16x2(lop3_and_or(q8, 0x000F000Fu, 0x64006400u), zlo), s2);
+    a[4 * w + 3] = mul_f16x2(sub_f16x2(lop3_and_or(q8, 0x00F000F0u, 0x54005400u), zhi), s2);
+  }
+}
+
+// int8: 64 codes (group j of the row's 128-byte stage line) to fp16 code *
+// scale (grouped) or the exact code (per channel, scale applied later).  A
+// biased byte b = code + 128 becomes the fp16 1024 + b (exact), minus 1152.
+template <bool kScaled>
+__device__ __forceinline__ void dequant_w8(uint32_t row_addr, uint32_t m, int j, uint32_t s2,
+                                           uint32_t (&a)[32]) {
+  const uint32_t sw = m & 7u;
+  const uint32_t bias = 0x64806480u;                           // fp16x2 (1152, 1152)
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = lds128(row_addr + (((uint32_t)(4 * j + c) ^ sw) << 4));
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t u = words[w] ^ 0x80808080u;
+      uint32_t lo = sub_f16x2(__byte_perm(u, 0x64646464u, 0x4140u), bias);
+      uint32_t hi = sub_f16x2(__byte_perm(u, 0x64646464u, 0x4342u), bias);
+      if (kScaled) {
+        lo = mul_f16x2(lo, s2);
+        hi = mul_f16x2(hi, s2);
+      }
+      a[8 * c + 2 * w] = lo;
+      a[8 * c + 2 * w + 1] = hi;
+    }
+  }
+}
+
 template <int QUANT, int TPAD>
 __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
-  constexpr int S = C::kStages, NA = C::kNumA, NP = C::kNumP, SUB = C::kSub, SG = C::kSG;
+  constexpr int S = C::kStages, NA = C::kNumA, SUB = C::kSub;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -207,9 +213,9 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* a_full = empty + S;
   uint64_t* a_empty = a_full + NA;
-  uint64_t* p_full = a_empty + NA;
-  uint64_t* p_empty = p_full + NP;
-  uint64_t* wg_bar = p_empty + NP;
+  uint64_t* d_full = a_empty + NA;
+  uint64_t* d_empty = d_full + 2;
+  uint64_t* wg_bar = d_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* fix_flag = abort_flag + 1;
@@ -219,19 +225,20 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   const int G = gridDim.x;
   const long long begin = unit_begin(blockIdx.x, p.total, G);
   const long long end = unit_begin(blockIdx.x + 1, p.total, G);
+  const bool per_channel = (QUANT == kW8) && p.group_size == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::kDqWarps + SG + 4);   // dequant warps, MMA commits, epilogue warps
+      mbar_init(&empty[s], C::kDqWarps + kMmaWarps);   // dequant warps + MMA commits
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(&a_full[s], C::kDqWarps);
-      mbar_init(&a_empty[s], SG);
+      mbar_init(&a_empty[s], kMmaWarps);
     }
-    for (int s = 0; s < NP; ++s) {
-      mbar_init(&p_full[s], SG);
-      mbar_init(&p_empty[s], 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&d_full[b], kMmaWarps);
+      mbar_init(&d_empty[b], 4);
     }
     mbar_init(wg_bar, 4);
     *abort_flag = 0;
@@ -256,10 +263,10 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
 
   const long long nunits = end - begin;
   // valid 64-k groups of stage kst (the last stage of a row may be partial)
-  // and the scale/zero row of group jg inside the stage's box
+  // and the scale/zero row of group j inside the stage's box
   auto nsub_of = [&](int kst) { return min(SUB, (p.K - kst * C::kStageKK) >> 6); };
-  auto grow_of = [&](int kst, int jg) {
-    return p.group_size ? (((kst * C::kStageKK + 64 * jg) >> p.gshift) - ((kst * C::kStageKK) >> p.gshift))
+  auto grow_of = [&](int kst, int j) {
+    return p.group_size ? (((kst * C::kStageKK + 64 * j) >> p.gshift) - ((kst * C::kStageKK) >> p.gshift))
                         : 0;
   };
 
@@ -294,100 +301,132 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       }
     }
   } else if (warp < C::kMmaWarp0) {
-    // ------------------------------------------------------------ dequant
-    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
-    const int jj = (warp - C::kDqWarp0) >> 2;     // k group of each step this warp handles
-    const int m = q * 32 + lane;                  // weight row inside the tile
+    // ------------------------------------------------------------ dequant + activation conversion
+    const int dq = warp - C::kDqWarp0;
+    const int q = warp & 3;                   // TMEM lane quadrant this warp may access
+    const int jj = dq >> 2;                   // 64-k group of each stage this warp handles
+    const int m = q * 32 + lane;              // weight row inside the tile
     const uint32_t a_addr0 = tbase + ((uint32_t)(q * 32) << 16) + jj * 32;
     const uint32_t zshift = (m & 1) * 4;
+    const int xchunk0 = (dq * 32 + lane) * C::kXChunksPerLane;
+    float xmax = 0.f;
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
     Ring<NA> a_ring;
-    bool ok = true;
-    for (long long n = 0; ok && n < nunits; ++n, it.next(), st_ring.next()) {
+    for (long long n = 0; n < nunits; ++n, it.next(), st_ring.next(), a_ring.next()) {
       const int nsub = nsub_of(it.kst);
       const int s = st_ring.slot;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err))) break;
       const uint8_t* st = smem + s * C::kStageBytes;
-      const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
-      for (int ls = 0; ls * SG < nsub; ++ls, a_ring.next()) {
-        const int jg = ls * SG + jj;              // group inside the stage
-        uint32_t a[32];
-        if (jg < nsub) {
-          if constexpr (QUANT == kW4) {
-            const uint32_t zb = st[C::kZeroOff + grow_of(it.kst, jg) * 64 + (m >> 1)];
-            dequant_sub_w4(row_addr, m, jg, (zb >> zshift) & 0xFu, a);
-          } else {
-            dequant_sub_w8(row_addr, m, jg, a);
+      uint32_t a[32];
+      if (jj < nsub) {
+        const int grow = grow_of(it.kst, jj);
+        const __half sc = reinterpret_cast<const __half*>(st + C::kScaleOff)[grow * kTileM + m];
+        const uint32_t s2 = (uint32_t)__half_as_ushort(sc) * 0x00010001u;
+        const uint32_t row_addr = smem_u32(st + C::kCodeOff) + m * 128;
+        if constexpr (QUANT == kW4) {
+          const uint32_t zb = st[C::kZeroOff + grow * 64 + (m >> 1)];
+          dequant_w4(row_addr, m, jj, (zb >> zshift) & 0xFu, s2, a);
+        } else {
+          if (per_channel)
+            dequant_w8<false>(row_addr, m, jj, s2, a);
+          else
+            dequant_w8<true>(row_addr, m, jj, s2, a);
+        }
+      }
+      // this lane's share of the stage's activations: bf16 -> fp16 in place
+      {
+        const uint32_t xbase = smem_u32(st + C::kXOff);
+#pragma unroll
+        for (int c = 0; c < C::kXChunksPerLane; ++c) {
+          const int chunk = xchunk0 + c;
+          if (chunk * 16 < nsub * C::kXBoxBytes) {
+            const uint32_t addr = xbase + chunk * 16;
+            uint4 v = lds128(addr);
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(w[e] << 16);
+              const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+              xmax = fmaxf(xmax, fmaxf(fabsf(lo), fabsf(hi)));
+              w[e] = pack_f16x2(lo, hi);
+            }
+            sts128(addr, make_uint4(w[0], w[1], w[2], w[3]));
           }
         }
-        const int sa = a_ring.slot;
-        if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
-        if (jg < nsub) {
-          tc_fence_after();
-          tmem_st_32x32b_x32(a_addr0 + sa * C::kACols, a);
-          tmem_wait_st();
-          tc_fence_before();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[sa]);
+        fence_proxy_async_smem();
+      }
+      const int sa = a_ring.slot;
+      if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err))) break;
+      if (jj < nsub) {
+        tc_fence_after();
+        tmem_st_32x32b_x32(a_addr0 + sa * C::kACols, a);
+        tmem_wait_st();
+        tc_fence_before();
       }
       __syncwarp();
-      if (ok && lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        mbar_arrive(&a_full[sa]);
+        mbar_arrive(&empty[s]);
+      }
     }
+    // 65520 and above round to infinity in fp16
+    if (!(xmax < 65520.f)) atomicCAS(p.err, 0, kDevErrRange);
   } else if (warp < C::kEpWarp0) {
-    // ------------------------------------------------------------ MMA issue (k group jj)
+    // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      const int jj = warp - C::kMmaWarp0;
-      constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
+      const int mw = warp - C::kMmaWarp0;
+      constexpr uint32_t idesc = idesc_f16_f32(128, TPAD);
       UnitIter it(begin, p.ks);
       Ring<S> st_ring;
       Ring<NA> a_ring;
-      Ring<NP> p_ring;
-      bool ok = true, issued_any = false;
-      int last_sp = 0;
+      Ring<2> d_ring;
+      bool ok = true;
+      int last_sa = -1;
       uint32_t last_phase = 0;
-      for (long long n = 0; ok && n < nunits; ++n, it.next(), st_ring.next()) {
-        const int nsub = nsub_of(it.kst);
-        const int s = st_ring.slot;
-        if (!mbar_wait(&full[s], st_ring.phase, abort_flag, p.err)) break;
-        const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
-        for (int ls = 0; ls * SG < nsub; ++ls, a_ring.next(), p_ring.next()) {
-          const int sa = a_ring.slot, sp = p_ring.slot;
-          if (!mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err) ||
-              !mbar_wait(&p_empty[sp], p_ring.phase ^ 1, abort_flag, p.err)) {
+      long long n = 0;
+      while (ok && n < nunits) {
+        // one tile segment into accumulator buffer d_ring.slot
+        const long long tile_end = (long long)(it.tile + 1) * p.ks;
+        const long long seg_len = min(end, tile_end) - (begin + n);
+        const uint32_t d_col = tbase + C::kD0 + d_ring.slot * C::kDCols + mw * TPAD;
+        if (!mbar_wait(&d_empty[d_ring.slot], d_ring.phase, abort_flag, p.err)) break;
+        for (long long e = 0; e < seg_len; ++e, ++n, it.next(), st_ring.next(), a_ring.next()) {
+          const int nsub = nsub_of(it.kst);
+          const int s = st_ring.slot, sa = a_ring.slot;
+          if (!mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int jg = ls * SG + jj;
-          if (jg < nsub) {
-            const uint32_t a_col = tbase + sa * C::kACols + jj * 32;
-            const uint32_t d_col = tbase + C::kPCols0 + sp * C::kPCols + jj * TPAD;
-            const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
+          const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row
-              mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
+          for (int g = 0; g < C::kGroupsPerMma; ++g) {
+            const int jg = mw * C::kGroupsPerMma + g;
+            if (jg < nsub) {
+              const uint32_t a_col = tbase + sa * C::kACols + jg * 32;
+              const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                // A: 8 TMEM columns (16 fp16) per K16 step; B: +32 bytes inside the swizzled row.
+                // The accumulator is cleared by the epilogue, so every MMA accumulates.
+                mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, 1u);
+              }
             }
           }
           mma_commit(&a_empty[sa]);
-          mma_commit(&p_full[sp]);
-          issued_any = true;
-          last_sp = sp;
-          last_phase = p_ring.phase;
+          mma_commit(&empty[s]);
+          last_sa = sa;
+          last_phase = a_ring.phase;
         }
         if (!ok) break;
-        // the stage's shared memory may be reused once these MMAs are done
-        mma_commit(&empty[s]);
+        mma_commit(&d_full[d_ring.slot]);
+        d_ring.next();
       }
-      if (*abort_flag && issued_any) {
+      if (*abort_flag && last_sa >= 0) {
         // wait for this thread's own MMAs before the CTA frees its tensor memory
         volatile int no_abort = 0;
-        mbar_wait(&p_full[last_sp], last_phase, &no_abort, nullptr, kDrainLimitNs);
+        mbar_wait(&a_empty[last_sa], last_phase, &no_abort, nullptr, kDrainLimitNs);
       }
     }
   } else {
@@ -403,14 +442,24 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       wg_phase ^= 1;
       return __all_sync(0xffffffffu, ok);
     };
-
-    float acc[TPAD];
+    auto clear_d = [&](int b) {
+      uint32_t zeros32[32];
 #pragma unroll
-    for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-    bool ok = true;
+      for (int c = 0; c < 32; ++c) zeros32[c] = 0u;
+#pragma unroll
+      for (int c = 0; c < C::kDCols; c += 32)
+        tmem_st_32x32b_x32(tbase + lane_base + C::kD0 + b * C::kDCols + c, zeros32);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[b]);
+    };
+    clear_d(0);
+    clear_d(1);
+
     UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    Ring<NP> p_ring;
+    Ring<2> d_ring;
+    bool ok = true;
     long long n = 0;
     while (ok && n < nunits) {
       const int tile = it.tile;
@@ -418,59 +467,43 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       const long long u0 = begin + n;
       const long long seg_end = min(end, tile_first + p.ks);
       const bool whole_tile = (u0 == tile_first) && (seg_end == tile_first + p.ks);
-      for (long long u = u0; u < seg_end; ++u, ++n, it.next(), st_ring.next()) {
-        const int kst = it.kst;
-        const int nsub = nsub_of(kst);
-        const int s = st_ring.slot;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err));
-        if (!ok) break;
-        float sc[SUB];
-        {
-          const __half* srow = reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff);
+      for (long long u = u0; u < seg_end; ++u, ++n) it.next();
+      const int b = d_ring.slot;
+      ok = __all_sync(0xffffffffu, mbar_wait(&d_full[b], d_ring.phase, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int nrow = tile * kTileM + m;
+      const float osc = per_channel && nrow < p.N ? __half2float(__ushort_as_half(p.scales[nrow])) : 1.f;
+      const uint32_t dbase = tbase + lane_base + C::kD0 + b * C::kDCols;
+      // sum of the MMA warps' accumulators, 16 columns at a time
+      auto load_chunk = [&](int h, float (&v)[16]) {
+        uint32_t r0[16], r1[16];
+        tmem_ld_32x32b_x16(dbase + h * 16, r0);
+        tmem_ld_32x32b_x16(dbase + TPAD + h * 16, r1);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < SUB; ++j)
-            sc[j] = (j < nsub) ? __half2float(srow[grow_of(kst, j) * kTileM + m]) : 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        for (int c = 0; c < 16; ++c) v[c] = (__uint_as_float(r0[c]) + __uint_as_float(r1[c])) * osc;
+      };
+      if (whole_tile) {
 #pragma unroll
-        for (int ls = 0; ls < C::kSteps; ++ls) {
-          if (ls * SG >= nsub) break;
-          const int sp = p_ring.slot;
-          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[sp], p_ring.phase, abort_flag, p.err));
-          if (!ok) break;
-          tc_fence_after();
+        for (int h = 0; h < TPAD / 16; ++h) {
+          float v[16];
+          load_chunk(h, v);
+          if (nrow < p.N) {
 #pragma unroll
-          for (int jj = 0; jj < SG; ++jj) {
-            const int jg = ls * SG + jj;
-            if (jg < nsub) {
-              const uint32_t d_addr = tbase + lane_base + C::kPCols0 + sp * C::kPCols + jj * TPAD;
-              const float scj = sc[jg < SUB ? jg : 0];
-#pragma unroll
-              for (int h = 0; h < TPAD / 16; ++h) {
-                uint32_t rr[16];
-                tmem_ld_32x32b_x16(d_addr + h * 16, rr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 16; c += 2)
-                  fma_f32x2(acc[h * 16 + c], acc[h * 16 + c + 1], scj, __uint_as_float(rr[c]),
-                            __uint_as_float(rr[c + 1]));
+            for (int c = 0; c < 16; ++c) {
+              const int t = h * 16 + c;
+              if (t < p.T) {
+                if (p.y_f32)
+                  reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = v[c];
+                else
+                  reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(v[c]);
               }
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&p_empty[sp]);
-          p_ring.next();
         }
-        if (!ok) break;
-      }
-      if (!ok) break;
-
-      // ---- segment epilogue
-      const int nrow = tile * kTileM + m;
-      bool store = whole_tile;
-      if (!whole_tile) {
+        clear_d(b);
+      } else {
         // Split tile: add this CTA's partial into the tile's fp32 slot (keyed
         // by the tile's first contributor, unique per split tile); the last
         // contributor to arrive converts the sum and clears the slot.
@@ -478,7 +511,13 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
         const int c_last = cta_of_unit(tile_first + p.ks - 1, p.total, G);
         float* slot = p.partials + (size_t)c_first * kPartialSlotFloats;
 #pragma unroll
-        for (int t = 0; t < TPAD; ++t) red_add_f32(slot + t * kTileM + m, acc[t]);
+        for (int h = 0; h < TPAD / 16; ++h) {
+          float v[16];
+          load_chunk(h, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) red_add_f32(slot + (h * 16 + c) * kTileM + m, v[c]);
+        }
+        clear_d(b);
         __threadfence();
         ok = wg_sync();
         if (!ok) break;
@@ -488,13 +527,18 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
         }
         ok = wg_sync();
         if (!ok) break;
-        store = *fix_flag != 0;
-        if (store) {
+        if (*fix_flag) {
           __threadfence();
-#pragma unroll
+#pragma unroll 4
           for (int t = 0; t < TPAD; ++t) {
-            acc[t] = __ldcg(slot + t * kTileM + m);
+            const float v = __ldcg(slot + t * kTileM + m);
             __stcg(slot + t * kTileM + m, 0.f);
+            if (t < p.T && nrow < p.N) {
+              if (p.y_f32)
+                reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = v;
+              else
+                reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(v);
+            }
           }
           if (q == 0 && lane == 0) atomicExch(&p.counters[tile], 0);
         }
@@ -502,21 +546,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
         ok = wg_sync();
         if (!ok) break;
       }
-      if (store && nrow < p.N) {
-        if (p.y_f32) {
-          float* y = reinterpret_cast<float*>(p.y);
-#pragma unroll
-          for (int t = 0; t < TPAD; ++t)
-            if (t < p.T) y[(size_t)t * p.N + nrow] = acc[t];
-        } else {
-          __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.y);
-#pragma unroll
-          for (int t = 0; t < TPAD; ++t)
-            if (t < p.T) y[(size_t)t * p.N + nrow] = __float2bfloat16_rn(acc[t]);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
+      d_ring.next();
     }
   }
 
@@ -561,10 +591,10 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.gshift = 0;
   while (a.group_size && (1 << p.gshift) < a.group_size) ++p.gshift;
   p.ks = (a.K + C::kStageKK - 1) / C::kStageKK;
-  p.sr = sr;
   const long long tiles = (a.N + kTileM - 1) / kTileM;
   p.total = tiles * p.ks;
   p.tx = C::kSub * C::kXBoxBytes + C::kCodeBytes + sr * kTileM * 2 + (QUANT == kW4 ? sr * 64 : 0);
+  p.scales = a.scales;
   p.y = a.y;
   p.y_f32 = a.y_f32;
   p.partials = ctx->partials;

@@ -10,9 +10,9 @@ of the verify step, not part of it.
 
 Storage layouts (shared by the C ABI and the oracle):
 
-* int4 codes    uint8  [N][K/2]   each 4-byte word w of a row holds k = 8w..8w+7:
-                                   byte 4w+j carries k = 8w+j in its low nibble and
-                                   k = 8w+j+4 in its high nibble (j = 0..3)
+* int4 codes    uint8  [N][K/2]   each little-endian 32-bit word w of a row holds
+                                   k = 8w..8w+7, nibble p (from the least significant
+                                   end) holding k = 8w + 2*(p % 4) + p // 4
 * int4 scales   fp16   [K/g][N]   group-major (one row per quantisation group)
 * int4 zeros    uint8  [K/g][N/2] uint4 zero points, two output rows per byte,
                                    low nibble = even n
@@ -48,14 +48,16 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def pack_w4_codes(codes: np.ndarray) -> np.ndarray:
-    """Pack uint4 codes [..., K] (K % 8 == 0) into the int4 code layout: in
-    each group of eight consecutive k, byte j (j = 0..3) holds element j in
-    its low nibble and element j+4 in its high nibble."""
+    """Pack uint4 codes [..., K] (K % 8 == 0) into the int4 code layout: each
+    group of eight consecutive k becomes one little-endian 32-bit word whose
+    nibble p (from the least significant end) holds element 2*(p % 4) + p // 4,
+    i.e. bytes (k0 | k2<<4), (k4 | k6<<4), (k1 | k3<<4), (k5 | k7<<4)."""
     c = np.asarray(codes, dtype=np.uint8)
     K = c.shape[-1]
     assert K % 8 == 0
-    g = c.reshape(c.shape[:-1] + (K // 8, 8))
-    packed = (g[..., 0:4] & 0xF) | ((g[..., 4:8] & 0xF) << 4)
+    g = (c.reshape(c.shape[:-1] + (K // 8, 8)) & 0xF).astype(np.uint8)
+    packed = np.stack([g[..., 0] | (g[..., 2] << 4), g[..., 4] | (g[..., 6] << 4),
+                       g[..., 1] | (g[..., 3] << 4), g[..., 5] | (g[..., 7] << 4)], axis=-1)
     return packed.reshape(c.shape[:-1] + (K // 2,)).astype(np.uint8)
 
 

@@ -31,11 +31,13 @@
  * and tokens per pass": 4-bit asymmetric Medium tier, 8-bit symmetric Large
  * tier, one scale shared by every value of a group; the byte layouts are this
  * library's own):
- *   int4 codes   uint8 [N][K/2]   row n as 4-byte groups, one per 8 consecutive
- *                                 k: byte j (0..3) of group w holds k = 8w+j in
- *                                 its low nibble and k = 8w+j+4 in its high
- *                                 nibble (lets the kernel turn a byte pair into
- *                                 a bf16 pair with one permute)
+ *   int4 codes   uint8 [N][K/2]   row n as little-endian 32-bit words, one per
+ *                                 8 consecutive k: nibble p (from the least
+ *                                 significant end) of word w holds
+ *                                 k = 8w + 2*(p % 4) + p / 4, i.e. the bytes
+ *                                 carry (k0|k2<<4), (k4|k6<<4), (k1|k3<<4),
+ *                                 (k5|k7<<4) -- one mask turns a pair of
+ *                                 nibbles into an fp16 pair
  *   int4 scales  fp16  [K/g][N]   one row per quantisation group of g
  *                                 consecutive k
  *   int4 zeros   uint8 [K/g][N/2] uint4 zero points, low nibble = even n
@@ -67,7 +69,7 @@ enum spec_status {
   SPEC_ERR_CUDA = -4,     /* a CUDA runtime/driver call failed                 */
   SPEC_ERR_OOM = -5,      /* workspace allocation failed or is too small       */
   SPEC_ERR_TIMEOUT = -6,  /* a bounded device-side wait ran out (sticky)       */
-  SPEC_ERR_NUMERIC = -7   /* reserved: non-finite inputs                       */
+  SPEC_ERR_NUMERIC = -7   /* an input outside the supported numeric range      */
 };
 
 enum spec_dtype { SPEC_DTYPE_BF16 = 0, SPEC_DTYPE_F32 = 1 };
@@ -89,10 +91,12 @@ int spec_destroy(spec_ctx* ctx);
 
 /* Synchronise `stream`, then read and clear the context's device error word.
  * Returns SPEC_OK or the first device-side error recorded since the last call:
- * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_ARG when a draft
- * token (spec_accept) or parent index (spec_accept_tree) read on the device was
- * out of range (that draft/node was treated as rejected).  After an error the
- * split-K counters are re-zeroed so the context is usable again. */
+ * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_NUMERIC when a GEMM
+ * activation was outside the fp16 range, SPEC_ERR_ARG when a draft token
+ * (spec_accept) or parent index (spec_accept_tree) read on the device was out
+ * of range (that draft/node was treated as rejected).  After an error the
+ * split-K counters and partial sums are re-zeroed so the context is usable
+ * again. */
 int spec_sync_status(spec_ctx* ctx, void* stream);
 
 /* W4A16 verify GEMM ("How Uzu optimizes bytes and tokens per pass": Medium
@@ -104,9 +108,11 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size a power of two
  * >= 64 with K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or
  * SPEC_DTYPE_F32.
- * The (code - zero) factor is exact in bf16 and each group's partial sum is
- * scaled in fp32, so the only roundings are fp32 accumulation and the final
- * store. */
+ * Numerics: each weight (code - zero) * scale is rounded once to fp16
+ * (relative error <= 2^-11); activations are converted to fp16, exactly for
+ * |x| < 65520 (a larger value makes spec_sync_status report
+ * SPEC_ERR_NUMERIC and the output is then meaningless); products are
+ * accumulated in fp32. */
 int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
                 const uint8_t* zeros, int group_size, const uint16_t* x, void* y,
                 int y_dtype, int T, int N, int K, const int8_t* signs,
@@ -116,8 +122,10 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
  * checkpoint, 8-bit symmetric quantisation, no zero point).
  *   y[t][n] = sum_k x'[t][k] * code[n][k] * scale
  * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size a
- * power of two >= 64).  Rotation and sizes as qgemm_w4a16, except N % 8 == 0
- * suffices. */
+ * power of two >= 64).  Per-channel scales are applied exactly in fp32 to the
+ * accumulated sum; grouped weights are rounded once to fp16 like the int4
+ * path.  Activation range, rotation and sizes as qgemm_w4a16, except
+ * N % 8 == 0 suffices. */
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, const uint16_t* x, void* y, int y_dtype, int T,
                 int N, int K, const int8_t* signs, int hadamard_block,

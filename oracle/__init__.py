@@ -61,13 +61,17 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def unpack_w4_codes(qcodes: np.ndarray, N: int, K: int) -> np.ndarray:
-    """uint8 [N][K/2] -> int64 [N][K].  The row is read as groups of four
-    bytes, one group per eight consecutive k: byte j of a group holds the
-    group's element j in its low nibble and element j+4 in its high nibble."""
+    """uint8 [N][K/2] -> int64 [N][K].  The row is read as little-endian
+    32-bit words, one per eight consecutive k; nibble p of a word (counted
+    from the least significant end) holds the word's element 2*(p % 4) + p // 4,
+    so its four bytes carry (k0, k2), (k4, k6), (k1, k3), (k5, k7) as (low,
+    high) nibbles."""
     q = np.asarray(qcodes, dtype=np.uint8).reshape(N, K // 8, 4).astype(np.int64)
     out = np.empty((N, K // 8, 8), dtype=np.int64)
-    out[:, :, 0:4] = q & 0xF
-    out[:, :, 4:8] = q >> 4
+    for p in range(8):
+        byte, high = p // 2, p % 2
+        nib = (q[:, :, byte] >> 4) if high else (q[:, :, byte] & 0xF)
+        out[:, :, 2 * (p % 4) + p // 4] = nib
     return out.reshape(N, K)
 
 

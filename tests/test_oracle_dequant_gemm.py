@@ -16,11 +16,11 @@ def _f16(vals):
 
 
 def test_w4_dequant_hand_example():
-    # N=2 rows, K=8, groups of 4 along k.  Byte j of each 4-byte group holds
-    # element j (low nibble) and element j+4 (high nibble).
-    # row 0 codes [10, 3, 15, 0, 1, 2, 3, 4] -> bytes 0x1A, 0x23, 0x3F, 0x40
-    # row 1 codes [1, 2, 7, 8, 9, 10, 11, 12] -> bytes 0x91, 0xA2, 0xB7, 0xC8
-    qcodes = np.array([[0x1A, 0x23, 0x3F, 0x40], [0x91, 0xA2, 0xB7, 0xC8]], dtype=np.uint8)
+    # N=2 rows, K=8, groups of 4 along k.  The 4 bytes of a row's word carry
+    # (k0|k2<<4), (k4|k6<<4), (k1|k3<<4), (k5|k7<<4).
+    # row 0 codes [10, 3, 15, 0, 1, 2, 3, 4] -> bytes 0xFA, 0x31, 0x03, 0x42
+    # row 1 codes [1, 2, 7, 8, 9, 10, 11, 12] -> bytes 0x71, 0xB9, 0x82, 0xCA
+    qcodes = np.array([[0xFA, 0x31, 0x03, 0x42], [0x71, 0xB9, 0x82, 0xCA]], dtype=np.uint8)
     # zeros [G=2][N/2=1]: group 0 -> (n0=5, n1=1) = 0x15 ; group 1 -> (n0=0, n1=9) = 0x90
     zeros = np.array([[0x15], [0x90]], dtype=np.uint8)
     scales = _f16([[0.5, 2.0], [0.25, 1.0]])   # [G][N]
@@ -33,7 +33,7 @@ def test_w4_dequant_hand_example():
 def test_w4_generator_packing_matches_layout():
     codes = np.arange(16, dtype=np.uint8)[None, :] % 16   # k = 0..15
     packed = inputs.pack_w4_codes(codes)
-    assert list(packed[0]) == [0x40, 0x51, 0x62, 0x73, 0xC8, 0xD9, 0xEA, 0xFB]
+    assert list(packed[0]) == [0x20, 0x64, 0x31, 0x75, 0xA8, 0xEC, 0xB9, 0xFD]
 
 
 def test_w4_zero_points_zero_scales_one_gives_codes():
@@ -67,8 +67,10 @@ def _brute_w4(qcodes, scales, zeros, g, xbits, T, N, K):
     y = [[0.0] * N for _ in range(T)]
     for n in range(N):
         for k in range(K):
-            byte = int(qcodes[n, (k // 8) * 4 + (k % 4)])
-            code = (byte >> 4) if (k % 8) >= 4 else (byte & 0xF)
+            r = k % 8
+            pos = 4 * (r % 2) + r // 2          # nibble position inside the word
+            byte = int(qcodes[n, (k // 8) * 4 + pos // 2])
+            code = (byte >> 4) if pos % 2 else (byte & 0xF)
             zb = int(zeros[k // g, n // 2])
             zero = (zb >> 4) if (n & 1) else (zb & 0xF)
             w = (code - zero) * float(scales[k // g, n])

@@ -20,11 +20,11 @@
 //    weights never touch shared memory.  The same warps convert the stage's
 //    activations to fp16 in place (exact inside the fp16 range; a value
 //    outside it records an error);
-//  * two MMA warps (each issuing half of a stage's 64-k groups; several
-//    issuing warps are needed to keep the tensor core fed with small-N MMAs)
-//    accumulate D += A * B in fp32 across the whole tile segment, each into
-//    its own double-buffered TMEM accumulator;
-//  * four epilogue warps sum the two accumulators at the end of a segment
+//  * one MMA warp per 64-k group (several issuing warps are needed to keep
+//    the tensor core fed with small-N MMAs) accumulates D += A * B in fp32
+//    across the whole tile segment into its own TMEM accumulator (double
+//    buffered when TMEM allows);
+//  * four epilogue warps sum the accumulators at the end of a segment
 //    (times the per-channel scale for int8 without groups, which stays exact
 //    in fp32), clear them and write the output;
 //  * work is split stream-K style: the (tile, stage) units of the GEMM are
@@ -46,7 +46,6 @@ namespace sv {
 namespace {
 
 constexpr int kTmemCols = 512;
-constexpr int kMmaWarps = 2;
 
 template <int QUANT, int TPAD>
 struct Cfg {
@@ -65,14 +64,16 @@ struct Cfg {
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  // TMEM: a ring of A slots (one stage each, 32 columns per 64-k group) and
-  // two accumulator buffers, each holding one TPAD-column D per MMA warp.
+  // One MMA-issuing warp per 64-k group of a stage.  TMEM: a ring of A slots
+  // (one stage each, 32 columns per group) and one or two accumulator
+  // buffers, each holding one TPAD-column D per MMA warp.
+  static constexpr int kMmaWarps = kSub;
   static constexpr int kACols = 32 * kSub;
   static constexpr int kDCols = TPAD * kMmaWarps;
-  static constexpr int kNumAFit = (kTmemCols - 2 * kDCols) / kACols;
+  static constexpr int kDBufs = (2 * kDCols + 3 * kACols <= kTmemCols) ? 2 : 1;
+  static constexpr int kNumAFit = (kTmemCols - kDBufs * kDCols) / kACols;
   static constexpr int kNumA = kNumAFit > 4 ? 4 : kNumAFit;
   static constexpr int kD0 = kNumA * kACols;
-  static constexpr int kGroupsPerMma = kSub / kMmaWarps;
   // warps
   static constexpr int kDqWarps = 4 * kSub;
   static constexpr int kDqWarp0 = 1;
@@ -83,7 +84,7 @@ struct Cfg {
   static constexpr int kXChunksPerLane = (kSub * kXBoxBytes / 16) / (kDqWarps * 32);
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kNumA >= 2, "TMEM A ring too shallow");
-  static_assert(kD0 + 2 * kDCols <= kTmemCols, "TMEM budget");
+  static_assert(kD0 + kDBufs * kDCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kXChunksPerLane * kDqWarps * 32 * 16 == kSub * kXBoxBytes, "activation split");
 };
@@ -204,7 +205,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
-  constexpr int S = C::kStages, NA = C::kNumA, SUB = C::kSub;
+  constexpr int S = C::kStages, NA = C::kNumA, SUB = C::kSub, NDB = C::kDBufs;
+  constexpr int kMmaWarps = C::kMmaWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -214,8 +216,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   uint64_t* a_full = empty + S;
   uint64_t* a_empty = a_full + NA;
   uint64_t* d_full = a_empty + NA;
-  uint64_t* d_empty = d_full + 2;
-  uint64_t* wg_bar = d_empty + 2;
+  uint64_t* d_empty = d_full + NDB;
+  uint64_t* wg_bar = d_empty + NDB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* fix_flag = abort_flag + 1;
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       mbar_init(&a_full[s], C::kDqWarps);
       mbar_init(&a_empty[s], kMmaWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NDB; ++b) {
       mbar_init(&d_full[b], kMmaWarps);
       mbar_init(&d_empty[b], 4);
     }
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       UnitIter it(begin, p.ks);
       Ring<S> st_ring;
       Ring<NA> a_ring;
-      Ring<2> d_ring;
+      Ring<NDB> d_ring;
       bool ok = true;
       int last_sa = -1;
       uint32_t last_phase = 0;
@@ -400,9 +402,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
           }
           tc_fence_after();
           const uint64_t bdesc0 = smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff);
-#pragma unroll
-          for (int g = 0; g < C::kGroupsPerMma; ++g) {
-            const int jg = mw * C::kGroupsPerMma + g;
+          {
+            const int jg = mw;
             if (jg < nsub) {
               const uint32_t a_col = tbase + sa * C::kACols + jg * 32;
               const uint64_t bdesc = bdesc0 + (uint64_t)((jg * C::kXBoxBytes) >> 4);
@@ -454,11 +455,10 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&d_empty[b]);
     };
-    clear_d(0);
-    clear_d(1);
+    for (int b = 0; b < NDB; ++b) clear_d(b);
 
     UnitIter it(begin, p.ks);
-    Ring<2> d_ring;
+    Ring<NDB> d_ring;
     bool ok = true;
     long long n = 0;
     while (ok && n < nunits) {
@@ -477,12 +477,19 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       const uint32_t dbase = tbase + lane_base + C::kD0 + b * C::kDCols;
       // sum of the MMA warps' accumulators, 16 columns at a time
       auto load_chunk = [&](int h, float (&v)[16]) {
-        uint32_t r0[16], r1[16];
-        tmem_ld_32x32b_x16(dbase + h * 16, r0);
-        tmem_ld_32x32b_x16(dbase + TPAD + h * 16, r1);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = (__uint_as_float(r0[c]) + __uint_as_float(r1[c])) * osc;
+        for (int c = 0; c < 16; ++c) v[c] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; w += 2) {
+          uint32_t r0[16], r1[16];
+          tmem_ld_32x32b_x16(dbase + w * TPAD + h * 16, r0);
+          tmem_ld_32x32b_x16(dbase + (w + 1) * TPAD + h * 16, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r0[c]) + __uint_as_float(r1[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] *= osc;
       };
       if (whole_tile) {
 #pragma unroll

@@ -11,7 +11,6 @@ namespace sv {
 
 // Device-side error codes written into the context's error word.
 constexpr int kDevErrTimeout = 1;
-constexpr int kDevErrRange = 4;   // an activation did not fit the GEMM's fp16 operand range
 
 // A bounded wait gives up after this long (globaltimer nanoseconds) and
 // records kDevErrTimeout.  Legitimate waits inside one launch take
@@ -128,12 +127,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -226,13 +219,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);      // M / 16
 }
 
-// Same for fp16 A and B operands.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
-  return (1u << 4)                          // D format: f32
-         | ((uint32_t)(n >> 3) << 17)       // N / 8  (A, B format 0 = f16)
-         | ((uint32_t)(m >> 4) << 24);      // M / 16
-}
-
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
@@ -258,48 +244,23 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// (a0, a1) += s * (x0, x1) as one packed fp32x2 FMA.
-__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float s, float x0, float x1) {
-  uint64_t acc = (uint64_t)__float_as_uint(a0) | ((uint64_t)__float_as_uint(a1) << 32);
-  const uint64_t xs = (uint64_t)__float_as_uint(x0) | ((uint64_t)__float_as_uint(x1) << 32);
-  const uint64_t ss = (uint64_t)__float_as_uint(s) | ((uint64_t)__float_as_uint(s) << 32);
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(xs), "l"(ss));
-  a0 = __uint_as_float((uint32_t)acc);
-  a1 = __uint_as_float((uint32_t)(acc >> 32));
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
+// (a0, a1) - (b0, b1) as one packed fp32x2 subtraction.
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
-}
-
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

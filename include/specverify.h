@@ -69,7 +69,7 @@ enum spec_status {
   SPEC_ERR_CUDA = -4,     /* a CUDA runtime/driver call failed                 */
   SPEC_ERR_OOM = -5,      /* workspace allocation failed or is too small       */
   SPEC_ERR_TIMEOUT = -6,  /* a bounded device-side wait ran out (sticky)       */
-  SPEC_ERR_NUMERIC = -7   /* an input outside the supported numeric range      */
+  SPEC_ERR_NUMERIC = -7   /* reserved: no call of this version reports it      */
 };
 
 enum spec_dtype { SPEC_DTYPE_BF16 = 0, SPEC_DTYPE_F32 = 1 };
@@ -91,8 +91,7 @@ int spec_destroy(spec_ctx* ctx);
 
 /* Synchronise `stream`, then read and clear the context's device error word.
  * Returns SPEC_OK or the first device-side error recorded since the last call:
- * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_NUMERIC when a GEMM
- * activation was outside the fp16 range, SPEC_ERR_ARG when a draft token
+ * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_ARG when a draft token
  * (spec_accept) or parent index (spec_accept_tree) read on the device was out
  * of range (that draft/node was treated as rejected).  After an error the
  * split-K counters and partial sums are re-zeroed so the context is usable
@@ -108,11 +107,12 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size a power of two
  * >= 64 with K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or
  * SPEC_DTYPE_F32.
- * Numerics: each weight (code - zero) * scale is rounded once to fp16
- * (relative error <= 2^-11); activations are converted to fp16, exactly for
- * |x| < 65520 (a larger value makes spec_sync_status report
- * SPEC_ERR_NUMERIC and the output is then meaningless); products are
- * accumulated in fp32. */
+ * Numerics: the tensor cores multiply the exact integers (code - zero),
+ * held in bf16, by the bf16 activations as given, and sum each 64-k block in
+ * fp32; the block's fp16 scale is then applied in fp32 and the blocks are
+ * added in fp32.  Nothing is rounded before the sums, so the result differs
+ * from the exact product sum only by fp32 rounding of the additions (and the
+ * final rounding of a bf16 output).  Any finite bf16 activation is valid. */
 int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
                 const uint8_t* zeros, int group_size, const uint16_t* x, void* y,
                 int y_dtype, int T, int N, int K, const int8_t* signs,
@@ -122,10 +122,10 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
  * checkpoint, 8-bit symmetric quantisation, no zero point).
  *   y[t][n] = sum_k x'[t][k] * code[n][k] * scale
  * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size a
- * power of two >= 64).  Per-channel scales are applied exactly in fp32 to the
- * accumulated sum; grouped weights are rounded once to fp16 like the int4
- * path.  Activation range, rotation and sizes as qgemm_w4a16, except
- * N % 8 == 0 suffices. */
+ * power of two >= 64).  The int8 codes enter the tensor cores exactly (bf16
+ * holds -127..127); a per-channel scale multiplies the fp32 sum, grouped
+ * scales each 64-k block's fp32 sum, as in qgemm_w4a16.  Rotation and sizes
+ * as qgemm_w4a16, except N % 8 == 0 suffices. */
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, const uint16_t* x, void* y, int y_dtype, int T,
                 int N, int K, const int8_t* signs, int hadamard_block,

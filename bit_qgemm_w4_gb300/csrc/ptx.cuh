@@ -28,6 +28,21 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Let the next kernel on the stream (launched with programmatic stream
+// serialisation) be scheduled as soon as every CTA of this grid has called
+// this or exited.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel on the stream has completed and its memory
+// writes are visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void pdl_wait_prior() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

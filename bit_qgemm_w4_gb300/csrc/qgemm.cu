@@ -28,7 +28,13 @@
 //  * work is split stream-K style: the (tile, stage) units of the GEMM are
 //    divided evenly over the persistent grid; a tile cut between CTAs is
 //    summed with red.global.add into an fp32 slot and finished by the last
-//    contributor to arrive (no CTA ever waits for another).
+//    contributor to arrive (no CTA ever waits for another);
+//  * launches overlap: the kernel is launched with programmatic stream
+//    serialisation, lets the next kernel be scheduled at once, and waits for
+//    the previous kernel only before it reads activations or writes outputs
+//    and split-tile sums -- so a CTA that starts on an SM freed by the
+//    previous GEMM streams its first stages of weights (which no kernel
+//    writes) while that GEMM's last CTAs finish.
 // Every wait is bounded (see ptx.cuh); a timeout records an error, drains the
 // CTA's in-flight copies/MMAs and frees its tensor memory before returning.
 
@@ -258,6 +264,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  pdl_launch_dependents();
 
   const int nunits = end - begin;
   // valid 64-k groups of stage kst (only a tile's last stage may be partial)
@@ -269,7 +276,36 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     const uint64_t pol_w = policy_evict_first();
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
-    int n = 0;
+    // Weights, scales and zero points of the first ring's worth of stages go
+    // out before waiting for the previous kernel (no kernel writes them); the
+    // activation boxes of those stages follow once it has completed.
+    const int n_pre = nunits < S ? nunits : S;
+    if (lane == 0) {
+      UnitIter pit(begin, p.ks);
+      for (int n = 0; n < n_pre; ++n, pit.next()) {
+        const int nsub = nsub_of(pit.kst);
+        uint8_t* st = smem + n * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[n], p.tx - (SUB - nsub) * C::kXBoxBytes);
+        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[n], pit.kst * 128, pit.tile * kTileM, pol_w);
+        const int g0 = p.group_size ? (pit.kst * C::kStageKK) >> p.gshift : 0;
+        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[n], pit.tile * kTileM, g0);
+        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[n], pit.tile * (kTileM / 2), g0);
+      }
+      pdl_wait_prior();
+      pit = UnitIter(begin, p.ks);
+      for (int n = 0; n < n_pre; ++n, pit.next()) {
+        const int nsub = nsub_of(pit.kst);
+        uint8_t* st = smem + n * C::kStageBytes;
+        for (int j = 0; j < nsub; ++j)
+          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[n], pit.kst * C::kStageKK + 64 * j, 0);
+      }
+    }
+    __syncwarp();
+    for (int n = 0; n < n_pre; ++n) {
+      it.next();
+      st_ring.next();
+    }
+    int n = n_pre;
     for (; n < nunits; ++n, it.next(), st_ring.next()) {
       const int s = st_ring.slot;
       if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err))) break;
@@ -390,6 +426,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // outputs and split-tile sums may be read or cleared by the previous kernel
+    pdl_wait_prior();
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -596,8 +634,18 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
     if (rc) return rc;
     attr_done.fetch_or(bit);
   }
-  qgemm_kernel<QUANT, TPAD><<<(unsigned)G, C::kThreads, C::kSmemBytes, stream>>>(tx, tc, ts, tz, p);
-  return check_cuda(cudaGetLastError(), "qgemm launch");
+  // programmatic stream serialisation: see the design notes at the top
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return check_cuda(cudaLaunchKernelEx(&cfg, qgemm_kernel<QUANT, TPAD>, tx, tc, ts, tz, p), "qgemm launch");
 }
 
 template <int QUANT>

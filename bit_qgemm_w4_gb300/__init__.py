@@ -16,7 +16,7 @@ import os
 __all__ = [
     "SpecError", "Context", "lib", "spec_create", "spec_destroy", "spec_sync_status",
     "qgemm_w4a16", "qgemm_w8a16", "fwht_rotate", "spec_softmax", "spec_accept",
-    "spec_accept_tree", "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
+    "spec_accept_noalloc", "spec_accept_tree", "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
     "SPEC_DTYPE_BF16", "SPEC_DTYPE_F32",
 ]
 
@@ -41,6 +41,7 @@ _SIGS = {
     "fwht_rotate": [_P, _P, _P, _I, _I, _P, _I, _P],
     "spec_softmax": [_P, _P, _P, _I, _I, _P],
     "spec_accept": [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P],
+    "spec_accept_noalloc": [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P],
     "spec_accept_tree": [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P],
     "qdequant_w4": [_P, _P, _P, _P, _I, _I, _I, _P, _P],
     "qdequant_w8": [_P, _P, _P, _I, _I, _I, _P, _P],
@@ -168,6 +169,15 @@ def spec_accept(ctx, target_logits, draft_probs, draft_tokens, uniforms, T, V, n
     _call("spec_accept", _h(ctx), _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens),
           _ptr(uniforms), T, V, _ptr(n_accepted), _ptr(out_tokens), _ptr(near_tie_flags),
           _stream(stream))
+
+
+def spec_accept_noalloc(target_logits, draft_probs, draft_tokens, uniforms, T, V, n_accepted,
+                        out_tokens, near_tie_flags=None, device_status=None, stream=None) -> None:
+    """spec_accept on the current device with no context and no device allocation
+    (T <= 64; see the header for who needs it and how concurrent calls race)."""
+    _call("spec_accept_noalloc", _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens),
+          _ptr(uniforms), T, V, _ptr(n_accepted), _ptr(out_tokens), _ptr(near_tie_flags),
+          _ptr(device_status), _stream(stream))
 
 
 def spec_accept_tree(ctx, target_logits, draft_tokens, parent, T, V, path_len, out_tokens,

@@ -24,6 +24,7 @@
 
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "internal.hpp"
 
@@ -548,6 +549,119 @@ int launch_accept_tree(spec_ctx* ctx, const float* logits, const int32_t* drafts
   dim3 g(a.nchunks, rows);
   tree_kernel<<<g, kBlock, 0, s>>>(a);
   return check_cuda(cudaGetLastError(), "tree launch");
+}
+
+// ---------------------------------------------------------------- without allocation
+//
+// The same two launches as launch_accept, with their scratch taken from a
+// fixed array in this module's static device memory instead of a context's
+// workspace, for callers that cannot allocate device memory (see
+// spec_accept_noalloc in the public header).  Up to kNoAllocMaxT drafts.
+
+namespace {
+
+constexpr int kNoAllocMaxT = 64;
+constexpr size_t kNoAllocStatsBytes = sizeof(double) * 2 * (size_t)(kNoAllocMaxT + 1) * kAcceptChunks;
+constexpr size_t kNoAllocChunkBytes = sizeof(double) * kScanBlocks;
+// stats | chunk sums | arrival counter, error word (the last two start at zero)
+constexpr size_t kNoAllocScratchBytes = kNoAllocStatsBytes + kNoAllocChunkBytes + 2 * sizeof(int);
+
+static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+struct NoAllocSetup {
+  unsigned char* scratch;   // device address of g_accept_scratch
+  int num_sms;
+};
+
+}  // namespace
+
+// Device address of the static scratch and the SM count of the current
+// device, looked up once per device (with that device current).
+static int noalloc_setup(NoAllocSetup* out) {
+  static std::mutex mu;
+  static NoAllocSetup table[kMaxDevices] = {};
+  int dev = -1;
+  int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= kMaxDevices) return set_error(SPEC_ERR_ARG, "device %d outside 0..%d", dev, kMaxDevices - 1);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!table[dev].scratch) {
+    int major = 0, minor = 0, nsm = 0;
+    rc = check_cuda(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "device attribute");
+    if (rc) return rc;
+    rc = check_cuda(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "device attribute");
+    if (rc) return rc;
+    if (major != 10 || minor != 3)
+      return set_error(SPEC_ERR_CUDA, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+    rc = check_cuda(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev), "device attribute");
+    if (rc) return rc;
+    void* p = nullptr;
+    rc = check_cuda(cudaGetSymbolAddress(&p, g_accept_scratch), "cudaGetSymbolAddress(acceptance scratch)");
+    if (rc) return rc;
+    table[dev].scratch = static_cast<unsigned char*>(p);
+    table[dev].num_sms = nsm;
+  }
+  *out = table[dev];
+  return SPEC_OK;
+}
+
+int launch_accept_noalloc(const float* logits, const float* q, const int32_t* drafts, const float* u,
+                          int T, int V, int32_t* n_acc, int32_t* tokens, int32_t* flags,
+                          int32_t* status, cudaStream_t s) {
+  if (T > kNoAllocMaxT)
+    return set_error(SPEC_ERR_SHAPE,
+                     "spec_accept_noalloc takes at most %d drafts (its static scratch is sized for "
+                     "that); T=%d -- use spec_accept with a context instead",
+                     kNoAllocMaxT, T);
+  NoAllocSetup su;
+  int rc = noalloc_setup(&su);
+  if (rc) return rc;
+  double* stats = reinterpret_cast<double*>(su.scratch);
+  double* chunks = reinterpret_cast<double*>(su.scratch + kNoAllocStatsBytes);
+  int* counter = reinterpret_cast<int*>(su.scratch + kNoAllocStatsBytes + kNoAllocChunkBytes);
+  int* err = counter + 1;
+  // the arrival counter and the error word must start at zero
+  rc = check_cuda(cudaMemsetAsync(counter, 0, 2 * sizeof(int), s), "clear acceptance scratch");
+  if (rc) return rc;
+
+  const int rows = T + 1;
+  long long want = (4LL * su.num_sms + rows - 1) / rows;
+  long long by_size = ((long long)V + 1023) / 1024;
+  long long nc = want < by_size ? want : by_size;
+  if (nc < 1) nc = 1;
+  if (nc > kAcceptChunks) nc = kAcceptChunks;
+  dim3 g((unsigned)nc, rows);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, (int)nc, stats);
+  rc = check_cuda(cudaGetLastError(), "row_stats launch");
+  if (rc) return rc;
+  AcceptArgs a;
+  a.logits = logits;
+  a.q = q;
+  a.drafts = drafts;
+  a.u = u;
+  a.T = T;
+  a.V = V;
+  a.nstat = (int)nc;
+  a.stats = stats;
+  long long ns = ((long long)V + 1023) / 1024;
+  if (ns > kScanBlocks) ns = kScanBlocks;
+  if (ns < 1) ns = 1;
+  a.nscan = (int)ns;
+  a.chunk_sums = chunks;
+  a.counter = counter;
+  a.n_acc = n_acc;
+  a.tokens = tokens;
+  a.flags = flags;
+  a.err = err;
+  accept_kernel<<<a.nscan, kBlock, 0, s>>>(a);
+  rc = check_cuda(cudaGetLastError(), "accept launch");
+  if (rc) return rc;
+  if (status)
+    rc = check_cuda(cudaMemcpyAsync(status, err, sizeof(int), cudaMemcpyDeviceToDevice, s),
+                    "copy acceptance status");
+  return rc;
 }
 
 }  // namespace sv

@@ -347,6 +347,28 @@ int spec_accept(spec_ctx* ctx, const float* target_logits, const float* draft_pr
                        out_tokens, near_tie_flags, static_cast<cudaStream_t>(stream));
 }
 
+int spec_accept_noalloc(const float* target_logits, const float* draft_probs,
+                        const int32_t* draft_tokens, const float* uniforms, int T, int V,
+                        int32_t* n_accepted, int32_t* out_tokens, int32_t* near_tie_flags,
+                        int32_t* device_status, void* stream) {
+  clear_error();
+  if (T < 0) return set_error(SPEC_ERR_SHAPE, "T=%d is negative", T);
+  if (V < 1 || V > (1 << 26)) return set_error(SPEC_ERR_SHAPE, "V=%d outside 1..2^26", V);
+  SV_TRY(check_ptr(target_logits, 4, "target_logits"));
+  if (T > 0) {
+    SV_TRY(check_ptr(draft_probs, 4, "draft_probs"));
+    SV_TRY(check_ptr(draft_tokens, 4, "draft_tokens"));
+  }
+  SV_TRY(check_ptr(uniforms, 4, "uniforms"));
+  SV_TRY(check_ptr(n_accepted, 4, "n_accepted"));
+  SV_TRY(check_ptr(out_tokens, 4, "out_tokens"));
+  if (near_tie_flags) SV_TRY(check_ptr(near_tie_flags, 4, "near_tie_flags"));
+  if (device_status) SV_TRY(check_ptr(device_status, 4, "device_status"));
+  return launch_accept_noalloc(target_logits, draft_probs, draft_tokens, uniforms, T, V, n_accepted,
+                               out_tokens, near_tie_flags, device_status,
+                               static_cast<cudaStream_t>(stream));
+}
+
 int spec_accept_tree(spec_ctx* ctx, const float* target_logits, const int32_t* draft_tokens,
                      const int32_t* parent, int T, int V, int32_t* path_len, int32_t* out_tokens,
                      int32_t* path_nodes, void* stream) {

@@ -75,6 +75,9 @@ int launch_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows, i
 int launch_accept(spec_ctx* ctx, const float* logits, const float* q, const int32_t* drafts,
                   const float* u, int T, int V, int32_t* n_acc, int32_t* tokens, int32_t* flags,
                   cudaStream_t s);
+int launch_accept_noalloc(const float* logits, const float* q, const int32_t* drafts, const float* u,
+                          int T, int V, int32_t* n_acc, int32_t* tokens, int32_t* flags,
+                          int32_t* status, cudaStream_t s);
 int launch_accept_tree(spec_ctx* ctx, const float* logits, const int32_t* drafts,
                        const int32_t* parent, int T, int V, int32_t* path_len, int32_t* tokens,
                        int32_t* nodes, cudaStream_t s);

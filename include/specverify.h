@@ -170,6 +170,33 @@ int spec_accept(spec_ctx* ctx, const float* target_logits,
                 const float* uniforms, int T, int V, int32_t* n_accepted,
                 int32_t* out_tokens, int32_t* near_tie_flags, void* stream);
 
+/* spec_accept without a context and without allocating device memory.
+ * The pages describe nothing like it: it exists for callers that cannot
+ * allocate -- a process whose device memory is reserved by another
+ * allocator, a caller that must avoid the device-wide synchronisation that
+ * cudaMalloc/cudaFree can bring, or a component that owns no spec_ctx.
+ * The scratch the two acceptance kernels need (per-row softmax partials,
+ * residual chunk sums, an arrival counter and an error word, 68 KB) is a
+ * fixed array in the library's static device memory, which is why T is
+ * limited to 64 drafts here (a larger T is rejected with SPEC_ERR_SHAPE);
+ * nothing is allocated and nothing is freed.
+ * Runs on the calling thread's current device.  The first call on a device
+ * looks up the scratch's device address (cudaGetSymbolAddress) and the SM
+ * count; make that first call before any stream capture.  Every call clears
+ * the counter and error word on `stream` before its kernels.
+ * All calls on one device share the scratch: calls whose kernels may
+ * overlap (different streams without ordering between them, or several host
+ * threads) race and give wrong results -- keep them ordered on one stream.
+ * Arguments, layouts, sizes (except T <= 64) and results are those of
+ * spec_accept.  device_status (nullable, device int32 [1]) receives 0, or 2
+ * when a draft token was outside [0, V) (that draft then counts as
+ * rejected); spec_sync_status does not see this entry's errors. */
+int spec_accept_noalloc(const float* target_logits, const float* draft_probs,
+                        const int32_t* draft_tokens, const float* uniforms,
+                        int T, int V, int32_t* n_accepted, int32_t* out_tokens,
+                        int32_t* near_tie_flags, int32_t* device_status,
+                        void* stream);
+
 /* Greedy tree acceptance ("Karpathy's Trick ...", section "Issue with parallel
  * draft generation": the main model verifies the tree and accepts the longest
  * valid path; "Local LLM 4x Faster ...": verify the entire tree at once).

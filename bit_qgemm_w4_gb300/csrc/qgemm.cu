@@ -158,12 +158,15 @@ struct UnitIter {
 // fraction bits); subtracting 128 + zero leaves the exact integer.
 // The line was written by TMA with the 128-byte swizzle: 16-byte chunk c of
 // row m sits at chunk position c ^ (m & 7).
-__device__ __forceinline__ void dequant_w4(uint32_t row_addr, uint32_t m, int j, uint32_t z,
-                                           uint32_t (&a)[32]) {
+__device__ __forceinline__ void load_w4(uint32_t row_addr, uint32_t m, int j, uint32_t (&words)[8]) {
   const uint32_t sw = m & 7u;
   const uint4 c0 = lds128(row_addr + (((2u * j) ^ sw) << 4));
   const uint4 c1 = lds128(row_addr + (((2u * j + 1u) ^ sw) << 4));
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  words[0] = c0.x; words[1] = c0.y; words[2] = c0.z; words[3] = c0.w;
+  words[4] = c1.x; words[5] = c1.y; words[6] = c1.z; words[7] = c1.w;
+}
+
+__device__ __forceinline__ void dequant_w4(const uint32_t (&words)[8], uint32_t z, uint32_t (&a)[32]) {
   const uint32_t zz = (0x4300u | z) * 0x00010001u;             // bf16x2 (128 + z)
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
@@ -353,16 +356,27 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       const uint8_t* st = smem + s * C::kStageBytes;
       const int sa = a_ring.slot;
       bool ok = true;
-      // one group at a time: dequantise into registers, then store to TMEM
+      // all of this stage's shared-memory reads first (one exposed latency),
+      // then one group at a time: dequantise into registers, store to TMEM
       // (the first store waits for the A slot to be free; one wait for both)
+      uint32_t words[C::kGroupsPerDq][8];
+      uint32_t zb[C::kGroupsPerDq];
+      if constexpr (QUANT == kW4) {
+#pragma unroll
+        for (int i = 0; i < C::kGroupsPerDq; ++i) {
+          if (j0 + i < nsub) {
+            load_w4(smem_u32(st) + row_off, m, j0 + i, words[i]);
+            zb[i] = st[zero_off[i]];
+          }
+        }
+      }
 #pragma unroll
       for (int i = 0; i < C::kGroupsPerDq; ++i) {
         const int j = j0 + i;
         uint32_t a[32];
         if (j < nsub) {
           if constexpr (QUANT == kW4) {
-            const uint32_t zb = st[zero_off[i]];
-            dequant_w4(smem_u32(st) + row_off, m, j, (zb >> zshift) & 0xFu, a);
+            dequant_w4(words[i], (zb[i] >> zshift) & 0xFu, a);
           } else {
             dequant_w8(smem_u32(st) + row_off, m, j, a);
           }
@@ -439,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       wg_phase ^= 1;
       return __all_sync(0xffffffffu, ok);
     };
-    constexpr int kW = 16;                   // columns per tcgen05.ld (register budget)
+    constexpr int kW = TPAD < 32 ? TPAD : 32;   // columns read per wait (register budget)
 
     float acc[TPAD];
 #pragma unroll
@@ -484,7 +498,9 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < TPAD; c0 += kW) {
               uint32_t r[kW];
-              tmem_ld_32x32b_x16(dbase + j * TPAD + c0, r);
+#pragma unroll
+              for (int h = 0; h < kW / 16; ++h)
+                tmem_ld_32x32b_x16(dbase + j * TPAD + c0 + h * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[h * 16]));
               tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < kW; ++c) acc[c0 + c] = fmaf(sc[j], __uint_as_float(r[c]), acc[c0 + c]);

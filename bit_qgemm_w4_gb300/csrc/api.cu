@@ -111,7 +111,7 @@ WsLayout layout_for(int num_sms) {
   };
   L.slots = 4 * num_sms;   // two partial slots per CTA, two CTAs per SM
   L.err = take(256);
-  L.counters = take(sizeof(int) * (size_t)kMaxTiles);
+  L.counters = take(sizeof(int) * 4 * (size_t)kMaxTiles);
   L.partials = take(sizeof(float) * (size_t)kPartialSlotFloats * L.slots);
   L.xrot = take(sizeof(uint16_t) * (size_t)kMaxT * kMaxK);
   L.stats = take(sizeof(double) * 2 * (size_t)4096 * kAcceptChunks);
@@ -260,7 +260,7 @@ int spec_sync_status(spec_ctx* ctx, void* stream) {
   SV_TRY(check_cuda(cudaMemcpy(&err, ctx->err, sizeof(int), cudaMemcpyDeviceToHost), "read error word"));
   if (err == 0) return SPEC_OK;
   cudaMemset(ctx->err, 0, sizeof(int));
-  cudaMemset(ctx->tile_counters, 0, sizeof(int) * (size_t)kMaxTiles);
+  cudaMemset(ctx->tile_counters, 0, sizeof(int) * 4 * (size_t)kMaxTiles);
   cudaMemset(ctx->partials, 0, sizeof(float) * (size_t)kPartialSlotFloats * ctx->max_slots);
   cudaMemset(ctx->acc_counters, 0, sizeof(int) * 16);
   cudaDeviceSynchronize();

@@ -55,7 +55,7 @@ struct spec_ctx {
   size_t ws_bytes = 0;
   uint8_t* ws = nullptr;
   int* err = nullptr;             // device error word
-  int* tile_counters = nullptr;   // [kMaxTiles] split-K arrival counters
+  int* tile_counters = nullptr;   // [kMaxTiles][4] split-K arrival counters (per lane quadrant)
   float* partials = nullptr;      // [max_slots][kPartialSlotFloats]
   int max_slots = 0;
   uint16_t* xrot = nullptr;       // [kMaxT][kMaxK] rotated activations

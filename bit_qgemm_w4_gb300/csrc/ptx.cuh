@@ -255,8 +255,29 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return d;
 }
 
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+// p[0..3] += v[0..3] as one 16-byte vector reduction in L2 (p 16-byte aligned).
+__device__ __forceinline__ void red_add_f32x4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Atomic add with acquire-release semantics at GPU scope.  Issued by one lane
+// after a warp barrier it publishes every lane's earlier writes (release is
+// cumulative) and, for the thread that sees the final count, makes the other
+// contributors' writes visible (acquire).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// 16-byte load that bypasses L1 (sees other SMs' completed writes).
+__device__ __forceinline__ float4 ldcg_f32x4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {

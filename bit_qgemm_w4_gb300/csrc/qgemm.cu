@@ -221,10 +221,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   uint64_t* a_empty = a_full + NA;
   uint64_t* d_full = a_empty + NA;
   uint64_t* d_empty = d_full + ND;
-  uint64_t* wg_bar = d_empty + ND;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wg_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(d_empty + ND);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* fix_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -247,9 +245,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       mbar_init(&d_full[b], kMmaWarps);
       mbar_init(&d_empty[b], 4);
     }
-    mbar_init(wg_bar, 4);
     *abort_flag = 0;
-    *fix_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -445,14 +441,6 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t wg_phase = 0;
-    auto wg_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(wg_bar);
-      const bool ok = mbar_wait(wg_bar, wg_phase, abort_flag, p.err);
-      wg_phase ^= 1;
-      return __all_sync(0xffffffffu, ok);
-    };
     constexpr int kW = TPAD < 32 ? TPAD : 32;   // columns read per wait (register budget)
 
     float acc[TPAD];
@@ -533,50 +521,56 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
           }
         }
       } else {
-        // Split tile: add this CTA's partial into the tile's fp32 slot (keyed
-        // by the tile's first contributor, unique per split tile); the last
-        // contributor to arrive converts the sum and clears the slot.
+        // Split tile: add this warp's 32 rows of the CTA's partial into the
+        // tile's fp32 slot (keyed by the tile's first contributor, unique per
+        // split tile).  Arrivals are counted per lane quadrant, so each warp
+        // finishes its own rows: the last to arrive converts the sum and
+        // clears the slot, with no barrier between the epilogue warps.
         const int c_first = cta_of_unit(tile_first, p.total, G);
         const int c_last = cta_of_unit(tile_first + p.ks - 1, p.total, G);
-        float* slot = p.partials + (size_t)c_first * kPartialSlotFloats;
+        // slot layout [128 rows][TPAD]: a thread's values are contiguous, so
+        // the sums travel as 16-byte vector reductions and loads
+        float* slot = p.partials + (size_t)c_first * kPartialSlotFloats + (size_t)m * TPAD;
 #pragma unroll
-        for (int t = 0; t < TPAD; ++t) red_add_f32(slot + t * kTileM + m, v[t]);
-        __threadfence();
-        ok = wg_sync();
-        if (!ok) break;
-        if (q == 0 && lane == 0) {
-          const int old = atomicAdd(&p.counters[tile], 1);
-          *fix_flag = (old == c_last - c_first) ? 1 : 0;
-        }
-        ok = wg_sync();
-        if (!ok) break;
-        if (*fix_flag) {
-          __threadfence();
-          // 16 independent L2 reads before any store: the stores may alias the
-          // slot as far as the compiler knows, so interleaving them would
-          // serialise one L2 round trip per position.
+        for (int t = 0; t < TPAD; t += 4)
+          if (t < p.T) red_add_f32x4(slot + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomic_add_acq_rel_gpu(&p.counters[tile * 4 + q], 1) == c_last - c_first;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();   // orders lane 0's acquire before the other lanes' reads
+        if (last) {
+          // every read before any store (one L2 round trip for T <= 32): the
+          // stores may alias the slot as far as the compiler knows
+          constexpr int kB = TPAD % 32 == 0 ? 32 : 16;
 #pragma unroll
-          for (int h = 0; h < TPAD / 16; ++h) {
-            float w[16];
+          for (int h = 0; h < TPAD / kB; ++h) {
+            float4 w[kB / 4];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) w[c] = __ldcg(slot + (h * 16 + c) * kTileM + m);
+            for (int c = 0; c < kB / 4; ++c)
+              w[c] = (h * kB + 4 * c < p.T) ? ldcg_f32x4(slot + h * kB + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int t = h * 16 + c;
-              __stcg(slot + t * kTileM + m, 0.f);
-              if (t < p.T && nrow < p.N) {
-                if (p.y_f32)
-                  reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = w[c];
-                else
-                  reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(w[c]);
+            for (int c = 0; c < kB / 4; ++c) {
+              const int t0 = h * kB + 4 * c;
+              if (t0 < p.T) {
+                __stcg(reinterpret_cast<float4*>(slot + t0), make_float4(0.f, 0.f, 0.f, 0.f));
+                const float wv[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int t = t0 + e;
+                  if (t < p.T && nrow < p.N) {
+                    if (p.y_f32)
+                      reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = wv[e];
+                    else
+                      reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(wv[e]);
+                  }
+                }
               }
             }
           }
-          if (q == 0 && lane == 0) atomicExch(&p.counters[tile], 0);
+          // only this warp touches the counter until the kernel ends
+          if (lane == 0) __stcg(&p.counters[tile * 4 + q], 0);
         }
-        // keep fix_flag stable until every warp has read it
-        ok = wg_sync();
-        if (!ok) break;
       }
     }
   }

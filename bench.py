@@ -586,6 +586,44 @@ def run_kernel_case(args):
     ctx.close()
 
 
+def run_accept_case(args):
+    """spec_accept alone at T drafts over V tokens, launched warm-up + steps
+    times eagerly (for profiling the acceptance kernels in isolation); prints
+    its device time per call and the logits' read rate."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    T, V = (int(v) for v in args.accept_case.split(","))
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    a = inputs.accept_inputs(np.random.default_rng(11), T, V, logit_std=3.0, alpha=1.0, noise_std=0.5)
+    logits = torch.from_numpy(a.logits).to(dev)
+    q = torch.from_numpy(a.q).to(dev)
+    d = torch.from_numpy(a.drafts).to(dev)
+    u = torch.from_numpy(a.u).to(dev)
+    n = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(T + 1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        sv.spec_accept(ctx, logits, q, d, u, T, V, n, tok)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        sv.spec_accept(ctx, logits, q, d, u, T, V, n, tok)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = (T + 1) * V * 4
+    print(json.dumps({"accept_case": [T, V], "ms_per_call": round(ms, 6),
+                      "logits_GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "logits_bytes": nbytes}),
+          flush=True)
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -597,9 +635,14 @@ def main():
                     help="seconds of oracle GEMM work in the CPU baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="host seconds the reference arm spends on warm-up + timed steps")
+    ap.add_argument("--accept-case", default=None, metavar="T,V",
+                    help="time spec_accept alone at T drafts over V tokens (eager launches)")
     ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
                     help="time one int4 GEMM shape in isolation instead of the verify step")
     args = ap.parse_args()
+    if args.accept_case:
+        run_accept_case(args)
+        return
     if args.kernel_case:
         run_kernel_case(args)
     elif args.impl == "reference":

@@ -51,12 +51,6 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   return {M, a.s * (double)expf(a.m - M) + b.s * (double)expf(b.m - M)};
 }
 
-__device__ __forceinline__ MS ms_add(MS a, float x) {
-  if (x > a.m) return {x, a.s * (double)expf(a.m - x) + 1.0};
-  if (x == -INFINITY) return a;
-  return {a.m, a.s + (double)expf(x - a.m)};
-}
-
 // Sum over the block in a fixed order (deterministic).
 __device__ double block_sum(double v, double* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -97,6 +91,33 @@ __device__ MS block_ms(MS v, MS* sh) {
   return r;
 }
 
+// Inclusive prefix sum over the block's threads in a fixed order
+// (deterministic): a shuffle scan inside each warp, then over the warp totals.
+__device__ double block_incl_scan(double v, double* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __syncthreads();
+  if (lane == 31) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    double w = lane < kBlock / 32 ? sh[lane] : 0.0;
+#pragma unroll
+    for (int o = 1; o < kBlock / 32; o <<= 1) {
+      const double n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < kBlock / 32) sh[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) v += sh[warp - 1];
+  __syncthreads();
+  return v;
+}
+
 __device__ __forceinline__ void chunk_range(int c, int nchunks, int V, int& lo, int& hi) {
   const long long cs = ((long long)V + nchunks - 1) / nchunks;
   lo = (int)min((long long)V, (long long)c * cs);
@@ -112,8 +133,25 @@ __global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restri
   int lo, hi;
   chunk_range(c, nchunks, V, lo, hi);
   const float* l = logits + (long long)row * V;
-  MS a{-INFINITY, 0.0};
-  for (int v = lo + threadIdx.x; v < hi; v += kBlock) a = ms_add(a, __ldg(l + v));
+  // Per thread: online max and a compensated (Kahan) fp32 sum of
+  // exp(l - max), so its error stays near one fp32 rounding of the thread's
+  // total however many terms it holds; threads and chunks then combine in
+  // fp64.  (GB300's fp64 pipe is slow: one fp64 add per element would bound
+  // this pass, not the bytes.)
+  // (two passes over the thread's elements, the second from L1: its max,
+  // then the sum, with no rescaling)
+  float m = -INFINITY;
+  for (int v = lo + threadIdx.x; v < hi; v += kBlock) m = fmaxf(m, __ldg(l + v));
+  float sum = 0.f, comp = 0.f;
+  if (m != -INFINITY) {
+    for (int v = lo + threadIdx.x; v < hi; v += kBlock) {
+      const float y = expf(__ldg(l + v) - m) - comp;
+      const float t = sum + y;
+      comp = (t - sum) - y;
+      sum = t;
+    }
+  }
+  MS a{m, (double)sum - (double)comp};
   a = block_ms(a, sh);
   if (threadIdx.x == 0) {
     stats[((long long)row * nchunks + c) * 2 + 0] = a.m;
@@ -189,35 +227,56 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
   __shared__ double s_gap;
   __shared__ int s_flag[kMaxAcceptT + 1];
   __shared__ double s_pref[kScanBlocks + 1];
-  __shared__ double s_sub[kBlock + 1];
 
   const int T = a.T, V = a.V;
-  for (int r = threadIdx.x; r <= T; r += kBlock) {
-    const MS t = row_total(a.stats, r, a.nstat);
-    rowM[r] = t.m;
-    rowInvZ[r] = 1.0 / t.s;
+  {
+    // each row's chunk pairs merged by one warp (lanes over chunks)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r <= T; r += kBlock / 32) {
+      MS t{-INFINITY, 0.0};
+      for (int c = lane; c < a.nstat; c += 32) {
+        const MS x{(float)__ldcg(a.stats + ((long long)r * a.nstat + c) * 2),
+                   __ldcg(a.stats + ((long long)r * a.nstat + c) * 2 + 1)};
+        t = ms_merge(t, x);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const MS w{__shfl_xor_sync(0xffffffffu, t.m, o), __shfl_xor_sync(0xffffffffu, t.s, o)};
+        t = ms_merge(t, w);
+      }
+      if (lane == 0) {
+        rowM[r] = t.m;
+        rowInvZ[r] = 1.0 / t.s;
+      }
+    }
+  }
+  __syncthreads();
+  // every draft's test at once (one round of loads), then the left-to-right
+  // scan for the first rejection
+  for (int i = threadIdx.x; i < T; i += kBlock) {
+    const int x = a.drafts[i];
+    double p = 0.0, qx = 1.0;
+    const bool in_range = x >= 0 && x < V;
+    if (in_range) {
+      p = (double)expf(a.logits[(long long)i * V + x] - rowM[i]) * rowInvZ[i];
+      qx = (double)a.q[(long long)i * V + x];
+    }
+    const double r = qx == 0.0 ? (double)INFINITY : p / qx;
+    const double ui = (double)a.u[i];
+    // bit 0: accepted; bit 1: near tie; bit 2: out of range (rejected, reported)
+    s_flag[i] = (ui < fmin(1.0, r) ? 1 : 0) | (fabs(ui - r) < kTieEps ? 2 : 0) | (in_range ? 0 : 4);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int j = T;
     for (int i = 0; i < T; ++i) {
-      const int x = a.drafts[i];
-      double p = 0.0, qx = 1.0;
-      if (x >= 0 && x < V) {
-        p = (double)expf(a.logits[(long long)i * V + x] - rowM[i]) * rowInvZ[i];
-        qx = (double)a.q[(long long)i * V + x];
-      } else {
-        atomicCAS(a.err, 0, kDevErrBadToken);   // out-of-range draft: rejected, reported
-      }
-      const double r = qx == 0.0 ? (double)INFINITY : p / qx;
-      const double ui = (double)a.u[i];
-      s_flag[i] = fabs(ui - r) < kTieEps ? 1 : 0;
-      if (!(ui < fmin(1.0, r))) {
+      if (s_flag[i] & 4) atomicCAS(a.err, 0, kDevErrBadToken);
+      if (!(s_flag[i] & 1)) {
         j = i;
         break;
       }
     }
-    for (int i = j + 1; i < T; ++i) s_flag[i] = 0;
+    for (int i = 0; i < T; ++i) s_flag[i] = (i <= j && (s_flag[i] & 2)) ? 1 : 0;
     s_j = j;
   }
   __syncthreads();
@@ -260,38 +319,33 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
       }
       __syncthreads();
     }
-    if (threadIdx.x == 0) {
-      double acc = 0.0;
-      s_pref[0] = 0.0;
-      for (int c = 0; c < a.nscan; ++c) {
-        acc += __ldcg(a.chunk_sums + c);
-        s_pref[c + 1] = acc;
-      }
+    {
+      // prefix of the chunk sums (nscan <= kBlock): one block-wide scan
+      const double x = threadIdx.x < a.nscan ? __ldcg(a.chunk_sums + threadIdx.x) : 0.0;
+      const double incl = block_incl_scan(x, shf);
+      if (threadIdx.x < a.nscan) s_pref[threadIdx.x + 1] = incl;
+      if (threadIdx.x == 0) s_pref[0] = 0.0;
     }
     __syncthreads();
     if (s_pref[a.nscan] > 0.0 || attempt == 1) break;
   }
   const double Z = s_pref[a.nscan];
   const double target = (double)a.u[T] * Z;
+  // chosen chunk: the first with mass whose prefix passes the target (or, by
+  // rounding only, the last chunk with mass)
   if (threadIdx.x == 0) {
-    int cstar = -1;
-    for (int c = 0; c < a.nscan; ++c)
-      if (s_pref[c + 1] > target && s_pref[c + 1] > s_pref[c]) {
-        cstar = c;
-        break;
-      }
-    if (cstar < 0)   // rounding: last chunk with mass
-      for (int c = a.nscan - 1; c >= 0; --c)
-        if (s_pref[c + 1] > s_pref[c]) {
-          cstar = c;
-          break;
-        }
-    s_j = cstar < 0 ? 0 : cstar;   // reuse as the chosen chunk
+    s_j = 0x7fffffff;
+    s_last = -1;
     s_tok = 0x7fffffff;
     s_gap = 0.0;
   }
   __syncthreads();
-  const int cstar = s_j;
+  if (threadIdx.x < a.nscan && s_pref[threadIdx.x + 1] > s_pref[threadIdx.x]) {
+    if (s_pref[threadIdx.x + 1] > target) atomicMin(&s_j, (int)threadIdx.x);
+    atomicMax(&s_last, (int)threadIdx.x);
+  }
+  __syncthreads();
+  const int cstar = s_j != 0x7fffffff ? s_j : (s_last >= 0 ? s_last : 0);
   chunk_range(cstar, a.nscan, V, lo, hi);
   const int len = hi - lo;
   const int per = (len + kBlock - 1) / kBlock;
@@ -299,18 +353,9 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
   const int my_hi = min(hi, my_lo + per);
   double sub = 0.0;
   for (int v = my_lo; v < my_hi; ++v) sub += dr.w(v);
-  s_sub[threadIdx.x] = sub;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double acc = s_pref[cstar];
-    for (int t = 0; t < kBlock; ++t) {
-      const double x = s_sub[t];
-      s_sub[t] = acc;   // exclusive prefix
-      acc += x;
-    }
-  }
-  __syncthreads();
-  double cum = s_sub[threadIdx.x];
+  // this thread's starting cumulative weight: the chunk's prefix plus the
+  // exclusive prefix of the threads before it
+  double cum = s_pref[cstar] + (block_incl_scan(sub, shf) - sub);
   int cand = 0x7fffffff;
   double cgap = 0.0;
   for (int v = my_lo; v < my_hi; ++v) {

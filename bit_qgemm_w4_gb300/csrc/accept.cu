@@ -70,13 +70,22 @@ __device__ double block_sum(double v, double* sh) {
   return r;
 }
 
+// (max, sum) pairs of a warp merged with few fp64 operations (GB300's fp64
+// pipe is slow): the max over the warp in fp32, each lane's sum rescaled to
+// it once, then an fp64 butterfly sum.  Lane 0's result is the one used.
+__device__ __forceinline__ MS warp_ms(MS v) {
+  float M = v.m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  double sum = (M == -INFINITY || v.m == -INFINITY) ? 0.0 : v.s * (double)expf(v.m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  return {M, sum};
+}
+
 __device__ MS block_ms(MS v, MS* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-    v = ms_merge(v, w);
-  }
+  v = warp_ms(v);
   __syncthreads();
   if (lane == 0) sh[warp] = v;
   __syncthreads();
@@ -127,8 +136,11 @@ __device__ __forceinline__ void chunk_range(int c, int nchunks, int V, int& lo, 
 // ---------------------------------------------------------------- row stats
 
 __global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restrict__ logits, int V,
-                                                           int nchunks, double* __restrict__ stats) {
+                                                           int nchunks, double* __restrict__ stats,
+                                                           double* __restrict__ rowstat,
+                                                           int* __restrict__ rowcnt) {
   __shared__ MS sh[kBlock / 32];
+  __shared__ int s_lastrow;
   const int c = blockIdx.x, row = blockIdx.y;
   int lo, hi;
   chunk_range(c, nchunks, V, lo, hi);
@@ -156,28 +168,35 @@ __global__ void __launch_bounds__(kBlock) row_stats_kernel(const float* __restri
   if (threadIdx.x == 0) {
     stats[((long long)row * nchunks + c) * 2 + 0] = a.m;
     stats[((long long)row * nchunks + c) * 2 + 1] = a.s;
+    __threadfence();
+    s_lastrow = atomicAdd(&rowcnt[row], 1) == nchunks - 1;
   }
-}
-
-__device__ __forceinline__ MS row_total(const double* stats, int row, int nchunks) {
-  MS t{-INFINITY, 0.0};
-  for (int c = 0; c < nchunks; ++c) {
-    const MS x{(float)__ldcg(stats + ((long long)row * nchunks + c) * 2),
-               __ldcg(stats + ((long long)row * nchunks + c) * 2 + 1)};
-    t = ms_merge(t, x);
+  __syncthreads();
+  // the row's last chunk to finish merges the row once: (max, 1/Z)
+  if (s_lastrow && threadIdx.x < 32) {
+    __threadfence();
+    MS t{-INFINITY, 0.0};
+    for (int k = threadIdx.x; k < nchunks; k += 32) {
+      const MS x{(float)__ldcg(stats + ((long long)row * nchunks + k) * 2),
+                 __ldcg(stats + ((long long)row * nchunks + k) * 2 + 1)};
+      t = ms_merge(t, x);
+    }
+    t = warp_ms(t);
+    if (threadIdx.x == 0) {
+      rowstat[row * 2 + 0] = (double)t.m;
+      rowstat[row * 2 + 1] = 1.0 / t.s;
+      rowcnt[row] = 0;
+    }
   }
-  return t;
 }
 
 __global__ void __launch_bounds__(kBlock) softmax_norm_kernel(const float* __restrict__ logits,
                                                               float* __restrict__ probs, int V,
                                                               int nchunks,
-                                                              const double* __restrict__ stats) {
-  __shared__ MS tot;
+                                                              const double* __restrict__ rowstat) {
   const int c = blockIdx.x, row = blockIdx.y;
-  if (threadIdx.x == 0) tot = row_total(stats, row, nchunks);
-  __syncthreads();
-  const float M = tot.m, invZ = (float)(1.0 / tot.s);
+  const float M = (float)__ldcg(rowstat + row * 2);
+  const float invZ = (float)__ldcg(rowstat + row * 2 + 1);
   int lo, hi;
   chunk_range(c, nchunks, V, lo, hi);
   const float* l = logits + (long long)row * V;
@@ -193,8 +212,7 @@ struct AcceptArgs {
   const int32_t* drafts;
   const float* u;        // [T+1]
   int T, V;
-  int nstat;             // chunks of row_stats
-  const double* stats;
+  const double* rowstat;  // [T+1][2] per-row (max, 1/Z)
   int nscan;             // blocks of accept_kernel == residual chunks
   double* chunk_sums;    // [nscan]
   int* counter;
@@ -229,26 +247,9 @@ __global__ void __launch_bounds__(kBlock) accept_kernel(AcceptArgs a) {
   __shared__ double s_pref[kScanBlocks + 1];
 
   const int T = a.T, V = a.V;
-  {
-    // each row's chunk pairs merged by one warp (lanes over chunks)
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r <= T; r += kBlock / 32) {
-      MS t{-INFINITY, 0.0};
-      for (int c = lane; c < a.nstat; c += 32) {
-        const MS x{(float)__ldcg(a.stats + ((long long)r * a.nstat + c) * 2),
-                   __ldcg(a.stats + ((long long)r * a.nstat + c) * 2 + 1)};
-        t = ms_merge(t, x);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const MS w{__shfl_xor_sync(0xffffffffu, t.m, o), __shfl_xor_sync(0xffffffffu, t.s, o)};
-        t = ms_merge(t, w);
-      }
-      if (lane == 0) {
-        rowM[r] = t.m;
-        rowInvZ[r] = 1.0 / t.s;
-      }
-    }
+  for (int r = threadIdx.x; r <= T; r += kBlock) {
+    rowM[r] = (float)__ldcg(a.rowstat + r * 2);
+    rowInvZ[r] = __ldcg(a.rowstat + r * 2 + 1);
   }
   __syncthreads();
   // every draft's test at once (one round of loads), then the left-to-right
@@ -534,10 +535,10 @@ int launch_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows, i
                    cudaStream_t s) {
   const int nc = stat_chunks(ctx, rows, V);
   dim3 g(nc, rows);
-  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats, ctx->acc_rowstat, ctx->acc_rowcnt);
   int rc = check_cuda(cudaGetLastError(), "row_stats launch");
   if (rc) return rc;
-  softmax_norm_kernel<<<g, kBlock, 0, s>>>(logits, probs, V, nc, ctx->acc_stats);
+  softmax_norm_kernel<<<g, kBlock, 0, s>>>(logits, probs, V, nc, ctx->acc_rowstat);
   return check_cuda(cudaGetLastError(), "softmax_norm launch");
 }
 
@@ -547,7 +548,7 @@ int launch_accept(spec_ctx* ctx, const float* logits, const float* q, const int3
   const int rows = T + 1;
   const int nc = stat_chunks(ctx, rows, V);
   dim3 g(nc, rows);
-  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, nc, ctx->acc_stats, ctx->acc_rowstat, ctx->acc_rowcnt);
   int rc = check_cuda(cudaGetLastError(), "row_stats launch");
   if (rc) return rc;
   AcceptArgs a;
@@ -557,8 +558,7 @@ int launch_accept(spec_ctx* ctx, const float* logits, const float* q, const int3
   a.u = u;
   a.T = T;
   a.V = V;
-  a.nstat = nc;
-  a.stats = ctx->acc_stats;
+  a.rowstat = ctx->acc_rowstat;
   long long ns = ((long long)V + 1023) / 1024;
   if (ns > kScanBlocks) ns = kScanBlocks;
   if (ns < 1) ns = 1;
@@ -608,8 +608,12 @@ namespace {
 constexpr int kNoAllocMaxT = 64;
 constexpr size_t kNoAllocStatsBytes = sizeof(double) * 2 * (size_t)(kNoAllocMaxT + 1) * kAcceptChunks;
 constexpr size_t kNoAllocChunkBytes = sizeof(double) * kScanBlocks;
-// stats | chunk sums | arrival counter, error word (the last two start at zero)
-constexpr size_t kNoAllocScratchBytes = kNoAllocStatsBytes + kNoAllocChunkBytes + 2 * sizeof(int);
+constexpr size_t kNoAllocRowBytes = sizeof(double) * 2 * (kNoAllocMaxT + 1);
+// stats | chunk sums | row (max, 1/Z) | arrival counter, error word, per-row
+// counters (these last start at zero)
+constexpr int kNoAllocZeroInts = 2 + kNoAllocMaxT + 1;
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocStatsBytes + kNoAllocChunkBytes + kNoAllocRowBytes + kNoAllocZeroInts * sizeof(int);
 
 static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 
@@ -665,10 +669,12 @@ int launch_accept_noalloc(const float* logits, const float* q, const int32_t* dr
   if (rc) return rc;
   double* stats = reinterpret_cast<double*>(su.scratch);
   double* chunks = reinterpret_cast<double*>(su.scratch + kNoAllocStatsBytes);
-  int* counter = reinterpret_cast<int*>(su.scratch + kNoAllocStatsBytes + kNoAllocChunkBytes);
+  double* rowstat = reinterpret_cast<double*>(su.scratch + kNoAllocStatsBytes + kNoAllocChunkBytes);
+  int* counter = reinterpret_cast<int*>(su.scratch + kNoAllocStatsBytes + kNoAllocChunkBytes + kNoAllocRowBytes);
   int* err = counter + 1;
-  // the arrival counter and the error word must start at zero
-  rc = check_cuda(cudaMemsetAsync(counter, 0, 2 * sizeof(int), s), "clear acceptance scratch");
+  int* rowcnt = counter + 2;
+  // the arrival counters and the error word must start at zero
+  rc = check_cuda(cudaMemsetAsync(counter, 0, kNoAllocZeroInts * sizeof(int), s), "clear acceptance scratch");
   if (rc) return rc;
 
   const int rows = T + 1;
@@ -678,7 +684,7 @@ int launch_accept_noalloc(const float* logits, const float* q, const int32_t* dr
   if (nc < 1) nc = 1;
   if (nc > kAcceptChunks) nc = kAcceptChunks;
   dim3 g((unsigned)nc, rows);
-  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, (int)nc, stats);
+  row_stats_kernel<<<g, kBlock, 0, s>>>(logits, V, (int)nc, stats, rowstat, rowcnt);
   rc = check_cuda(cudaGetLastError(), "row_stats launch");
   if (rc) return rc;
   AcceptArgs a;
@@ -688,8 +694,7 @@ int launch_accept_noalloc(const float* logits, const float* q, const int32_t* dr
   a.u = u;
   a.T = T;
   a.V = V;
-  a.nstat = (int)nc;
-  a.stats = stats;
+  a.rowstat = rowstat;
   long long ns = ((long long)V + 1023) / 1024;
   if (ns > kScanBlocks) ns = kScanBlocks;
   if (ns < 1) ns = 1;

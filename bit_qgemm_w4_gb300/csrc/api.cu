@@ -97,7 +97,8 @@ namespace {
 
 // Workspace layout (bytes, each region 256-aligned).
 struct WsLayout {
-  size_t err, counters, partials, xrot, stats, chunks, argidx, argval, acc_counters, total;
+  size_t err, counters, partials, xrot, stats, chunks, argidx, argval, acc_counters, rowstat, rowcnt,
+      total;
   int slots;
 };
 
@@ -119,6 +120,8 @@ WsLayout layout_for(int num_sms) {
   L.argidx = take(sizeof(int) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
   L.argval = take(sizeof(float) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
   L.acc_counters = take(sizeof(int) * 16);
+  L.rowstat = take(sizeof(double) * 2 * (size_t)4096);
+  L.rowcnt = take(sizeof(int) * (size_t)4096);
   L.total = off;
   return L;
 }
@@ -234,6 +237,8 @@ int spec_create(int device, size_t workspace_bytes, spec_ctx** out) {
   ctx->acc_argmax = reinterpret_cast<int*>(ctx->ws + L.argidx);
   ctx->acc_argval = reinterpret_cast<float*>(ctx->ws + L.argval);
   ctx->acc_counters = reinterpret_cast<int*>(ctx->ws + L.acc_counters);
+  ctx->acc_rowstat = reinterpret_cast<double*>(ctx->ws + L.rowstat);
+  ctx->acc_rowcnt = reinterpret_cast<int*>(ctx->ws + L.rowcnt);
   *out = ctx;
   return SPEC_OK;
 }
@@ -263,6 +268,7 @@ int spec_sync_status(spec_ctx* ctx, void* stream) {
   cudaMemset(ctx->tile_counters, 0, sizeof(int) * 4 * (size_t)kMaxTiles);
   cudaMemset(ctx->partials, 0, sizeof(float) * (size_t)kPartialSlotFloats * ctx->max_slots);
   cudaMemset(ctx->acc_counters, 0, sizeof(int) * 16);
+  cudaMemset(ctx->acc_rowcnt, 0, sizeof(int) * 4096);
   cudaDeviceSynchronize();
   if (err == 1) return set_error(SPEC_ERR_TIMEOUT, "a device-side wait timed out");
   return set_error(SPEC_ERR_ARG, "a draft token or parent index read on the device was out of "

@@ -64,6 +64,8 @@ struct spec_ctx {
   int* acc_argmax = nullptr;      // [kMaxAcceptT+1][kAcceptChunks] argmax partial index
   float* acc_argval = nullptr;    // [kMaxAcceptT+1][kAcceptChunks] argmax partial value
   int* acc_counters = nullptr;    // [16] arrival counters of the acceptance kernels
+  double* acc_rowstat = nullptr;  // [4096][2] per-row (max, 1/Z) merged by row_stats
+  int* acc_rowcnt = nullptr;      // [4096] per-row arrival counters of row_stats, kept zeroed
 };
 
 namespace sv {

@@ -56,6 +56,13 @@ def w4_gemm_bytes(T: int, N: int, K: int, g: int = GROUP, out_bytes: int = 2) ->
     return N * K // 2 + (K // g) * N * 2 + (K // g) * (N // 2) + T * K * 2 + T * N * out_bytes
 
 
+def w8_gemm_bytes(T: int, N: int, K: int, out_bytes: int = 2) -> int:
+    """Bytes a per-channel W8A16 GEMM must move: int8 codes, one fp16 scale per
+    output channel, bf16 activations in, outputs out (a rotation pre-pass adds
+    its own 4*T*K, counted separately)."""
+    return N * K + N * 2 + T * K * 2 + T * N * out_bytes
+
+
 def stack_bytes(T: int) -> int:
     return inputs.LAYERS_9B * sum(w4_gemm_bytes(T, N, K) for _, K, N in inputs.LAYER_9B)
 
@@ -586,6 +593,50 @@ def run_kernel_case(args):
     ctx.close()
 
 
+def run_kernel_case_w8(args):
+    """One per-channel W8A16 GEMM shape (optionally with the block random
+    Hadamard rotation of the activations, block B) launched warm-up + steps
+    times; prints its device time and achieved bandwidth."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    vals = [int(v) for v in args.kernel_case_w8.split(",")]
+    T, N, K = vals[:3]
+    B = vals[3] if len(vals) > 3 else 0
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    copies = max(1, min(16, (256 << 20) // max(1, N * K) + 1))
+    ws = [inputs.w8_weights_device(gen, N, K, dev) for _ in range(copies)]
+    x = inputs.activations_device(gen, T, K, dev)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    signs = torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(5), K)).to(dev) if B else None
+
+    def run(i):
+        w = ws[i % copies]
+        sv.qgemm_w8a16(ctx, w["qcodes"], w["scales"], 0, x, y, T, N, K, signs, B)
+
+    for i in range(args.warmup):
+        run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        run(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = w8_gemm_bytes(T, N, K)
+    print(json.dumps({"kernel_case_w8": [T, N, K, B], "copies": copies, "ms_per_launch": round(ms, 6),
+                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes}), flush=True)
+    ctx.close()
+
+
 def run_accept_case(args):
     """spec_accept alone at T drafts over V tokens, launched warm-up + steps
     times eagerly (for profiling the acceptance kernels in isolation); prints
@@ -637,11 +688,16 @@ def main():
                     help="host seconds the reference arm spends on warm-up + timed steps")
     ap.add_argument("--accept-case", default=None, metavar="T,V",
                     help="time spec_accept alone at T drafts over V tokens (eager launches)")
+    ap.add_argument("--kernel-case-w8", default=None, metavar="T,N,K[,B]",
+                    help="time one per-channel int8 GEMM shape (B > 0: rotation block)")
     ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
                     help="time one int4 GEMM shape in isolation instead of the verify step")
     args = ap.parse_args()
     if args.accept_case:
         run_accept_case(args)
+        return
+    if args.kernel_case_w8:
+        run_kernel_case_w8(args)
         return
     if args.kernel_case:
         run_kernel_case(args)

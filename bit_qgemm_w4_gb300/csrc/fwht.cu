@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.hpp"
+#include "ptx.cuh"
 
 namespace sv {
 namespace {
@@ -30,6 +31,9 @@ template <int R>
 __global__ void __launch_bounds__(256) fwht_kernel(const uint16_t* __restrict__ x, uint16_t* y,
                                                    int T, int K, const int8_t* __restrict__ signs,
                                                    float scale) {
+  // A GEMM launched after this pre-pass may start streaming its weights at
+  // once; it waits for this kernel before it reads the rotated activations.
+  pdl_launch_dependents();
   constexpr int B = 32 * R;
   const int lane = threadIdx.x & 31;
   const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);

@@ -365,6 +365,41 @@ def run_gpu(args):
     e1.record()
     torch.cuda.synchronize()
     t16_ms = e0.elapsed_time(e1) / K16
+
+    # ---- 27B-class Large tier: 64 layers of per-channel int8 projections at
+    # T=32 with the block-1024 random Hadamard rotation of the activations
+    L8 = inputs.LAYER_27B
+    w8 = [[inputs.w8_weights_device(gen, N, K, dev) for _, K, N in L8] for _ in range(inputs.LAYERS_27B)]
+    x8 = [inputs.activations_device(gen, T_MAIN, K, dev) for _, K, _ in L8]
+    y8 = [torch.empty((T_MAIN, N), dtype=torch.bfloat16, device=dev) for _, _, N in L8]
+    s8 = [torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(300 + j), K)).to(dev)
+          for j, (_, K, _) in enumerate(L8)]
+
+    def stack8():
+        for l in range(inputs.LAYERS_27B):
+            for j, (_, K, N) in enumerate(L8):
+                w = w8[l][j]
+                sv.qgemm_w8a16(ctx, w["qcodes"], w["scales"], 0, x8[j], y8[j], T_MAIN, N, K, s8[j], 1024)
+
+    stack8()
+    sv.spec_sync_status(ctx)
+    g_w8 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_w8, stream=side):
+            stack8()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g_w8.replay()
+    K8 = max(5, min(K, 20))
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K8):
+        g_w8.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    w8_ms = e0.elapsed_time(e1) / K8
+    w8_bytes = inputs.LAYERS_27B * sum(w8_gemm_bytes(T_MAIN, N, K) + 4 * T_MAIN * K for _, K, N in L8)
+    del w8
     clocks = sampler.stop()
     sv.spec_sync_status(ctx)
 
@@ -462,6 +497,17 @@ def run_gpu(args):
                 "unit": "GB/s",
                 "frac": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9 / peak, 4),
                 "draft_tokens_scored_per_s": round(T_SMALL / (t16_ms * 1e-3), 1),
+            },
+            "w8_27b": {
+                "workload": "27B-class int8 per-channel stack at T=32: 64 layers (qkv 5120x7168, "
+                            "o 5120x5120, gate_up 5120x34816, down 17408x5120), block-1024 random "
+                            "Hadamard rotation of every GEMM's activations (no head, no acceptance)",
+                "ms_per_step": round(w8_ms, 5),
+                "bytes_per_step": w8_bytes,
+                "value": round(w8_bytes / (w8_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
+                "frac": round(w8_bytes / (w8_ms * 1e-3) / 1e9 / peak, 4),
+                "draft_tokens_scored_per_s": round(T_MAIN / (w8_ms * 1e-3), 1),
             },
             "roofline": {
                 "kernel": "qgemm_kernel<W4, TPAD=32> (all 145 GEMM launches of a step)",

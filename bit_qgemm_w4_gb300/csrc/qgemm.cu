@@ -9,10 +9,12 @@
 //
 // Design (swap-AB: 128 weight rows are the MMA's M dimension, the T drafted
 // positions its N dimension; one CTA per SM owns all 512 TMEM columns):
-//  * a TMA warp streams stages into a shared-memory ring: per stage the
-//    128-byte line of codes of each of the 128 weight rows (256 k of int4 or
-//    128 k of int8 -- full-width HBM bursts), the stage's scale and zero
-//    rows, and the stage's bf16 activation boxes;
+//  * two TMA warps stream stages into a shared-memory ring: one issues per
+//    stage the 128-byte line of codes of each of the 128 weight rows (256 k
+//    of int4 or 128 k of int8 -- full-width HBM bursts) and the stage's scale
+//    and zero rows, the other the stage's bf16 activation boxes, each on its
+//    own barrier (one issuing thread that also issued the activation boxes
+//    kept too few weight bytes in flight to stream at full HBM rate);
 //  * eight dequantisation warps (two per TMEM lane quadrant, one weight row
 //    per thread) turn codes into exact bf16 integers (code - zero, or the
 //    int8 code) and write them straight into a TMEM ring with tcgen05.st --
@@ -32,9 +34,9 @@
 //  * launches overlap: the kernel is launched with programmatic stream
 //    serialisation, lets the next kernel be scheduled at once, and waits for
 //    the previous kernel only before it reads activations or writes outputs
-//    and split-tile sums -- so a CTA that starts on an SM freed by the
-//    previous GEMM streams its first stages of weights (which no kernel
-//    writes) while that GEMM's last CTAs finish.
+//    and split-tile sums -- the weight stream (which no kernel writes) never
+//    waits, so a CTA that starts on an SM freed by the previous GEMM fills
+//    its ring with weights while that GEMM's last CTAs finish.
 // Every wait is bounded (see ptx.cuh); a timeout records an error, drains the
 // CTA's in-flight copies/MMAs and frees its tensor memory before returning.
 
@@ -69,14 +71,16 @@ struct Cfg {
   static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  // warps: producer, dequant, MMA issue (one per 64-k group), epilogue
+  // warps: weight producer, dequant, MMA issue (one per 64-k group),
+  // epilogue, activation producer
   static constexpr int kDqWarps = 8;                            // two per TMEM lane quadrant
   static constexpr int kGroupsPerDq = kSub / 2;                 // 64-k groups of a stage per dequant warp
   static constexpr int kMmaWarps = kSub;
   static constexpr int kDqWarp0 = 1;
   static constexpr int kMmaWarp0 = kDqWarp0 + kDqWarps;
   static constexpr int kEpWarp0 = kMmaWarp0 + kMmaWarps;
-  static constexpr int kThreads = 32 * (kEpWarp0 + 4);
+  static constexpr int kXWarp = kEpWarp0 + 4;
+  static constexpr int kThreads = 32 * (kXWarp + 1);
   // TMEM: a ring of A slots (one stage each, 32 columns per group) and a ring
   // of partial sets (one stage each, TPAD columns per group).
   static constexpr int kACols = 32 * kSub;
@@ -86,10 +90,15 @@ struct Cfg {
   static constexpr int kNumAFit = (kTmemCols - kNumD * kDCols) / kACols;
   static constexpr int kNumA = kNumAFit > 4 ? 4 : kNumAFit;
   static constexpr int kD0 = kNumA * kACols;
+  // When the A ring is no deeper than the partial ring, the completion of
+  // stage n's MMAs (the partial ring's "full" barrier) also frees stage n's A
+  // slot, so the MMA warps commit one barrier per stage instead of two.
+  static constexpr bool kAFromD = kNumA <= kNumD;
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kNumA >= 2 && kNumD >= 1, "TMEM rings too shallow");
   static_assert(kD0 + kNumD * kDCols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert((3 * kStages + 2 * kNumA + 2 * kNumD) * 8 + 8 <= kCtrlBytes, "barrier block");
 };
 
 struct Params {
@@ -100,7 +109,7 @@ struct Params {
   int last_nsub;       // valid 64-k groups in a tile's last stage
   int gsh;             // row of group j in a stage's scale/zero box = (64 j) >> gsh
   int total;           // tiles * ks units (< 2^28)
-  uint32_t tx;         // TMA bytes per full stage
+  uint32_t tx_w;       // TMA bytes of a stage's codes, scales and zero points
   const uint16_t* scales;   // per-channel int8 scales (applied at the end of a segment)
   void* y;
   int y_f32;
@@ -221,7 +230,8 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   uint64_t* a_empty = a_full + NA;
   uint64_t* d_full = a_empty + NA;
   uint64_t* d_empty = d_full + ND;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(d_empty + ND);
+  uint64_t* x_full = d_empty + ND;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -234,8 +244,10 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      // released by the dequant warps, the MMA commits and the epilogue's scale reads
-      mbar_init(&empty[s], C::kDqWarps + kMmaWarps + 4);
+      mbar_init(&x_full[s], 1);
+      // released by the dequant warps and by the epilogue warps once the
+      // stage's MMAs have completed (they read the stage's scales)
+      mbar_init(&empty[s], C::kDqWarps + 4);
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(&a_full[s], C::kDqWarps);
@@ -270,55 +282,22 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
   auto nsub_of = [&](int kst) { return kst == p.ks - 1 ? p.last_nsub : SUB; };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight producer
     // (the whole warp walks the ring; lane 0 issues the copies)
     const uint64_t pol_w = policy_evict_first();
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
-    // Weights, scales and zero points of the first ring's worth of stages go
-    // out before waiting for the previous kernel (no kernel writes them); the
-    // activation boxes of those stages follow once it has completed.
-    const int n_pre = nunits < S ? nunits : S;
-    if (lane == 0) {
-      UnitIter pit(begin, p.ks);
-      for (int n = 0; n < n_pre; ++n, pit.next()) {
-        const int nsub = nsub_of(pit.kst);
-        uint8_t* st = smem + n * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[n], p.tx - (SUB - nsub) * C::kXBoxBytes);
-        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[n], pit.kst * 128, pit.tile * kTileM, pol_w);
-        const int g0 = p.group_size ? (pit.kst * C::kStageKK) >> p.gshift : 0;
-        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[n], pit.tile * kTileM, g0);
-        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[n], pit.tile * (kTileM / 2), g0);
-      }
-      pdl_wait_prior();
-      pit = UnitIter(begin, p.ks);
-      for (int n = 0; n < n_pre; ++n, pit.next()) {
-        const int nsub = nsub_of(pit.kst);
-        uint8_t* st = smem + n * C::kStageBytes;
-        for (int j = 0; j < nsub; ++j)
-          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[n], pit.kst * C::kStageKK + 64 * j, 0);
-      }
-    }
-    __syncwarp();
-    for (int n = 0; n < n_pre; ++n) {
-      it.next();
-      st_ring.next();
-    }
-    int n = n_pre;
+    int n = 0;
     for (; n < nunits; ++n, it.next(), st_ring.next()) {
       const int s = st_ring.slot;
       if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err))) break;
       if (lane == 0) {
-        const int nsub = nsub_of(it.kst);
         uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], p.tx - (SUB - nsub) * C::kXBoxBytes);
+        mbar_arrive_expect_tx(&full[s], p.tx_w);
         tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], it.kst * 128, it.tile * kTileM, pol_w);
         const int g0 = p.group_size ? (it.kst * C::kStageKK) >> p.gshift : 0;
         tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], it.tile * kTileM, g0);
         if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], it.tile * (kTileM / 2), g0);
-        for (int j = 0; j < nsub; ++j)
-          tma_load_2d(st + C::kXOff + j * C::kXBoxBytes, &tm_x, &full[s],
-                      it.kst * C::kStageKK + 64 * j, 0);
       }
       __syncwarp();
     }
@@ -345,6 +324,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     UnitIter it(begin, p.ks);
     Ring<S> st_ring;
     Ring<NA> a_ring;
+    Ring<ND> dprev;   // partial slot of stage n - NA (whose MMAs free this stage's A slot)
     for (int n = 0; n < nunits; ++n, it.next(), st_ring.next(), a_ring.next()) {
       const int nsub = nsub_of(it.kst);
       const int s = st_ring.slot;
@@ -378,7 +358,14 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
           }
         }
         if (i == 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err));
+          if constexpr (C::kAFromD) {
+            if (n >= NA) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&d_full[dprev.slot], dprev.phase, abort_flag, p.err));
+              dprev.next();
+            }
+          } else {
+            ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err));
+          }
           if (!ok) break;
           tc_fence_after();
         }
@@ -408,6 +395,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
       const int s = st_ring.slot, sa = a_ring.slot, b = d_ring.slot;
       if (!__all_sync(0xffffffffu, mbar_wait(&d_empty[b], d_ring.phase ^ 1, abort_flag, p.err))) break;
       if (!__all_sync(0xffffffffu, mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&x_full[s], st_ring.phase, abort_flag, p.err))) break;
       tc_fence_after();
       if (lane == 0) {
         if (jg < nsub_of(it.kst)) {
@@ -421,20 +409,19 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
             mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&a_empty[sa]);
-        mma_commit(&empty[s]);
+        if constexpr (!C::kAFromD) mma_commit(&a_empty[sa]);
         mma_commit(&d_full[b]);
       }
       __syncwarp();
-      last_sa = sa;
-      last_phase = a_ring.phase;
+      last_sa = b;
+      last_phase = d_ring.phase;
     }
     if (*abort_flag && last_sa >= 0 && lane == 0) {
       // wait for this warp's own MMAs before the CTA frees its tensor memory
       volatile int no_abort = 0;
-      mbar_wait(&a_empty[last_sa], last_phase, &no_abort, nullptr, kDrainLimitNs);
+      mbar_wait(&d_full[last_sa], last_phase, &no_abort, nullptr, kDrainLimitNs);
     }
-  } else {
+  } else if (warp < C::kXWarp) {
     // ------------------------------------------------------------ epilogue
     // outputs and split-tile sums may be read or cleared by the previous kernel
     pdl_wait_prior();
@@ -472,12 +459,12 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
           for (int j = 0; j < SUB; ++j)
             sc[j] = per_channel ? 1.f : __half2float(srow[((64 * j) >> p.gsh) * kTileM]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        // this stage's partials
+        // this stage's partials; once they are complete the stage's MMAs have
+        // finished reading its activations, so the slot can be released
         const int b = d_ring.slot;
         ok = __all_sync(0xffffffffu, mbar_wait(&d_full[b], d_ring.phase, abort_flag, p.err));
         if (!ok) break;
+        if (lane == 0) mbar_arrive(&empty[s]);
         tc_fence_after();
         const uint32_t dbase = tbase + lane_base + C::kD0 + b * C::kDCols;
 #pragma unroll
@@ -573,6 +560,32 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
         }
       }
     }
+  } else {
+    // ------------------------------------------------------------ activation producer
+    // (the activations may be written by the previous kernel; a slot is
+    // refilled once the epilogue has seen that stage's MMAs complete)
+    pdl_wait_prior();
+    UnitIter it(begin, p.ks);
+    Ring<S> st_ring;
+    int n = 0;
+    for (; n < nunits; ++n, it.next(), st_ring.next()) {
+      const int s = st_ring.slot;
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err))) break;
+      if (lane == 0) {
+        const int nsub = nsub_of(it.kst);
+        uint8_t* st = smem + s * C::kStageBytes + C::kXOff;
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(nsub * C::kXBoxBytes));
+        for (int j = 0; j < nsub; ++j)
+          tma_load_2d(st + j * C::kXBoxBytes, &tm_x, &x_full[s], it.kst * C::kStageKK + 64 * j, 0);
+      }
+      __syncwarp();
+    }
+    if (*abort_flag && lane == 0) {
+      for (int j = (n > S ? n - S : 0); j < n; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait(&x_full[j % S], (j / S) & 1, &no_abort, nullptr, kDrainLimitNs);
+      }
+    }
   }
 
   tc_fence_before();
@@ -620,7 +633,7 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   p.gsh = (a.group_size == 0 || a.group_size > C::kStageKK) ? 31 : p.gshift;
   const long long tiles = (a.N + kTileM - 1) / kTileM;
   p.total = tiles * p.ks;
-  p.tx = C::kSub * C::kXBoxBytes + C::kCodeBytes + sr * kTileM * 2 + (QUANT == kW4 ? sr * 64 : 0);
+  p.tx_w = C::kCodeBytes + sr * kTileM * 2 + (QUANT == kW4 ? sr * 64 : 0);
   p.scales = a.scales;
   p.y = a.y;
   p.y_f32 = a.y_f32;

@@ -293,6 +293,14 @@ __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// (a0 * b0 + c0, a1 * b1 + c1) as one packed instruction: two independent
+// round-to-nearest fp32 FMAs, bit-identical to two fmaf calls.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

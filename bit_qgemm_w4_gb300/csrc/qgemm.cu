@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    constexpr int kW = TPAD < 32 ? TPAD : 32;   // columns read per wait (register budget)
+    constexpr int kW = TPAD < 32 ? TPAD : (TPAD > 32 ? 16 : 32);   // columns read per wait (register budget)
 
     float acc[TPAD];
 #pragma unroll
@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < SUB; ++j) {
           if (j < nsub) {
+            const uint64_t s2 = pack_f32x2(__float_as_uint(sc[j]), __float_as_uint(sc[j]));
 #pragma unroll
             for (int c0 = 0; c0 < TPAD; c0 += kW) {
               uint32_t r[kW];
@@ -478,7 +479,13 @@ __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
                 tmem_ld_32x32b_x16(dbase + j * TPAD + c0 + h * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[h * 16]));
               tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < kW; ++c) acc[c0 + c] = fmaf(sc[j], __uint_as_float(r[c]), acc[c0 + c]);
+              for (int c = 0; c < kW; c += 2) {
+                // columns (t, t + 1) in one fma.rn.f32x2
+                const uint64_t d = fma_f32x2(s2, pack_f32x2(r[c], r[c + 1]),
+                                             pack_f32x2(__float_as_uint(acc[c0 + c]), __float_as_uint(acc[c0 + c + 1])));
+                acc[c0 + c] = __uint_as_float((uint32_t)d);
+                acc[c0 + c + 1] = __uint_as_float((uint32_t)(d >> 32));
+              }
             }
           }
         }

@@ -12,13 +12,14 @@
 // Launch structure (two launches for the chain rule, one for the tree):
 //  * row_stats_kernel: grid (chunks, rows); each block reduces one V-chunk of
 //    one row to an online-softmax pair (max, sum exp(l - max)) -- one pass over
-//    the logits, coalesced.
+//    the logits, coalesced; the last block of a row to arrive (per-row
+//    counter, no waiting) merges the row's pairs once and stores (max, 1/Z).
 //  * accept_kernel: grid = V-chunks of the single row that is sampled.  Every
-//    block merges the per-row pairs, replays the (at most T) sequential
-//    accept tests itself, and sums its chunk of the residual max(0, p_j - q_j)
-//    (or of p_T); the last block to arrive (atomic counter, no waiting) does
-//    the inverse-CDF draw: it picks the chunk from the chunk sums and scans
-//    that chunk only.
+//    block reads the rows' (max, 1/Z), runs the (at most T) accept tests in
+//    parallel and takes the first rejection, and sums its chunk of the
+//    residual max(0, p_j - q_j) (or of p_T); the last block to arrive (atomic
+//    counter, no waiting) does the inverse-CDF draw: it picks the chunk from
+//    the chunk sums by a block-wide scan and scans that chunk only.
 //  * tree_kernel: grid (chunks, T+1) argmax partials; the last block merges
 //    them and walks the tree.
 

@@ -25,6 +25,13 @@ argmax) standing in for a step where the definition is plain.  Sources:
 * "Local LLM 4x Faster--Not Through Hardware, but Through Speculative
   Decoding" (wink.run): random Hadamard transform for outliers; tree verify
   accepting the longest path.
+* The trymirai post feed (nitterts.pages.dev/trymirai), the post on the
+  "random number from 1 to 10" example: the speculator and the target both
+  sample with the same seed through the Gumbel-max trick, so matching
+  distributions give matching tokens.  The random numbers come from
+  Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+  easy as 1, 2, 3", SC 2011), a counter-based generator that the CUDA path
+  implements separately from the same published definition.
 
 Readings where the sources are silent (each is listed in the design doc):
 dequantisation w = (code - zero) * scale with groups of g consecutive k
@@ -32,7 +39,13 @@ inside one output row; Sylvester (natural-order) Hadamard with 1/sqrt(B);
 T+1 uniforms (u[0..T-1] for the accept tests, u[T] for the one final draw);
 strict u < min(1, p/q); inverse-CDF sampling in ascending token order;
 greedy tree rule (draft == argmax of the row that scores it), deepest node
-wins, ties to the smallest node index, argmax ties to the smallest token id.
+wins, ties to the smallest node index, argmax ties to the smallest token id;
+shared-seed rule: the noise of token v at draft position p is word v mod 4
+of Philox4x32-10 at counter (v div 4, p low, p high, 0) under key (seed low,
+seed high), made a uniform (2 floor(w / 2^9) + 1) / 2^24 and a Gumbel value
+-log(-log u); the target's token at position p is argmax_v (logit + noise),
+a draft is accepted while it equals that token, and the first position that
+differs (or position T) emits the target's token.
 
 Parity pins for every function live in tests/test_oracle_*.py.
 """
@@ -45,7 +58,8 @@ import numpy as np
 __all__ = [
     "bf16_bits_to_f64", "unpack_w4_codes", "unpack_w4_zeros", "dequant_w4",
     "dequant_w8", "hadamard", "rht", "qgemm_w4a16", "qgemm_w8a16", "softmax",
-    "spec_accept", "spec_accept_tree",
+    "spec_accept", "spec_accept_tree", "philox4x32_10", "gumbel_uniforms",
+    "gumbel_sample", "spec_accept_gumbel",
 ]
 
 
@@ -286,3 +300,108 @@ def spec_accept_tree(logits, drafts, parent):
     bonus = amax[best + 1] if best >= 0 else amax[0]
     tokens = [int(x[n]) for n in nodes] + [bonus]
     return len(nodes), np.asarray(tokens, dtype=np.int64), np.asarray(nodes, dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# shared-seed sampling (trymirai post feed, the post on sampling the
+# speculator and the LLM with the same seed via the Gumbel-max trick)
+# ----------------------------------------------------------------------------
+
+_PHILOX_MUL = (0xD2511F53, 0xCD9E8D57)     # round multipliers of Philox4x32
+_PHILOX_WEYL = (0x9E3779B9, 0xBB67AE85)    # key increments between rounds
+_U32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32-10 (Salmon et al., SC 2011) over an array of counters.
+
+    counter: integers [..., 4] (each < 2^32); key: (k0, k1).  One round takes
+    the products M0 * x0 and M1 * x2 (64-bit, exact in uint64) and gives the
+    next counter (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1,
+    lo(M0 x0)); between rounds the key grows by the Weyl constants (mod 2^32).
+    Returns uint32 [..., 4].
+    """
+    c = np.asarray(counter, dtype=np.uint64)
+    x0, x1, x2, x3 = (c[..., i].copy() for i in range(4))
+    k0, k1 = (int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF)
+    m0, m1 = np.uint64(_PHILOX_MUL[0]), np.uint64(_PHILOX_MUL[1])
+    for r in range(10):
+        if r > 0:
+            k0 = (k0 + _PHILOX_WEYL[0]) & 0xFFFFFFFF
+            k1 = (k1 + _PHILOX_WEYL[1]) & 0xFFFFFFFF
+        p0 = m0 * x0
+        p1 = m1 * x2
+        x0, x1, x2, x3 = ((p1 >> np.uint64(32)) ^ x1 ^ np.uint64(k0), p1 & _U32,
+                          (p0 >> np.uint64(32)) ^ x3 ^ np.uint64(k1), p0 & _U32)
+    return np.stack([x0, x1, x2, x3], axis=-1).astype(np.uint32)
+
+
+def gumbel_uniforms(seed: int, position: int, V: int) -> np.ndarray:
+    """The V uniforms of one draft position, in float64 (exact).
+
+    Token v takes word v mod 4 of Philox4x32-10 at counter (v div 4,
+    position mod 2^32, position div 2^32, 0) under key (seed mod 2^32,
+    seed div 2^32); a word w gives u = (2 floor(w / 2^9) + 1) / 2^24, an odd
+    multiple of 2^-24 strictly inside (0, 1).
+    """
+    seed = int(seed) % (1 << 64)
+    position = int(position) % (1 << 64)
+    nb = (V + 3) // 4
+    ctr = np.zeros((nb, 4), dtype=np.uint64)
+    ctr[:, 0] = np.arange(nb, dtype=np.uint64)
+    ctr[:, 1] = position & 0xFFFFFFFF
+    ctr[:, 2] = position >> 32
+    w = philox4x32_10(ctr, (seed & 0xFFFFFFFF, seed >> 32)).reshape(-1)[:V]
+    return (2.0 * (w.astype(np.float64) // 512.0) + 1.0) / float(1 << 24)
+
+
+def gumbel_sample(logits, seed: int, positions):
+    """One token per row by the Gumbel-max trick with shared noise.
+
+    Row r's token is argmax_v (logits[r][v] + g_v), g_v = -log(-log u_v) with
+    the uniforms of position positions[r] (smallest id among equal values).
+    Because g is a standard Gumbel variable, the token is distributed as
+    softmax(logits[r]).  Also returns each row's margin: its best value minus
+    the best value of any other token (0 on an exact tie).
+    """
+    l = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    if l.ndim == 1:
+        l = l[None, :]
+    R, V = l.shape
+    pos = [int(p) for p in np.atleast_1d(positions)]
+    assert len(pos) == R
+    tokens = np.zeros(R, dtype=np.int64)
+    margins = np.zeros(R, dtype=np.float64)
+    for r in range(R):
+        z = l[r] + (-np.log(-np.log(gumbel_uniforms(seed, pos[r], V))))
+        t = int(np.argmax(z))
+        tokens[r] = t
+        rest = np.delete(z, t)
+        margins[r] = z[t] - rest.max() if rest.size else math.inf
+    return tokens, margins
+
+
+def spec_accept_gumbel(logits, drafts, seed: int, position: int, tie_eps: float = 1e-4):
+    """Verification when the speculator sampled with the same seed.
+
+    logits [T+1][V]: row i scores draft position i (row T follows the last
+    draft).  The target's token at position i is the Gumbel-max sample of
+    row i with the noise of position `position + i`.  Drafts are accepted
+    left to right while they equal the target's token; the first position
+    that differs, or position T when all T are accepted, emits the target's
+    token.  A draft outside [0, V) never matches.
+
+    Returns (n_accepted, tokens[n_accepted + 1], near_tie[T + 1]) where
+    near_tie[i] marks a row whose margin is below tie_eps.
+    """
+    x = np.asarray(drafts, dtype=np.int64)
+    T = x.shape[0]
+    positions = [(int(position) + i) % (1 << 64) for i in range(T + 1)]
+    y, margins = gumbel_sample(logits, seed, positions)
+    n = T
+    for i in range(T):
+        if x[i] != y[i]:
+            n = i
+            break
+    tokens = np.concatenate([x[:n], [y[n]]]).astype(np.int64)
+    return n, tokens, margins < tie_eps

@@ -39,6 +39,7 @@ VOCAB = inputs.VOCAB_9B
 HIDDEN = 4096
 GROUP = 64
 ACCEPT_LEVELS = (0.3, 0.6, 0.9)
+GUMBEL_SEED = 0x5EED0000   # seed shared by the drafter and the verifier in the timed runs
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "verify-step HBM GB/s (% of peak) and draft tokens scored/s at T=16/32, int4 9B-class"
 WORKLOAD = ("9B-class int4 g64 verify step, T=32: 36 layers (qkv 4096x6144, o 4096x4096, "
@@ -75,6 +76,11 @@ def accept_bytes(T: int, V: int = VOCAB) -> int:
     """Target logits of all T+1 rows once, plus the one draft-probability row
     the final draw needs."""
     return (T + 1) * V * 4 + V * 4
+
+
+def accept_gumbel_bytes(T: int, V: int = VOCAB) -> int:
+    """Shared-seed acceptance: the logits once plus the drafts and outputs."""
+    return (T + 1) * V * 4 + T * 4 + (T + 2) * 4
 
 
 def step_bytes(T: int = T_MAIN) -> int:
@@ -366,6 +372,40 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t16_ms = e0.elapsed_time(e1) / K16
 
+    # ---- shared-seed (Gumbel-max) acceptance of the same T=32 blocks: the
+    # drafter's tokens are sampled on the GPU from log q with the same seed
+    # and positions as the verification (one launch over the logits)
+    gum = []
+    for i, a in enumerate(acc_sets):
+        logq = torch.from_numpy(np.log(a["host"].q).astype(np.float32)).to(dev)
+        d = torch.zeros(T_MAIN, dtype=torch.int32, device=dev)
+        sv.spec_gumbel_sample(ctx, logq, T_MAIN, VOCAB, GUMBEL_SEED + i, 0, d)
+        gum.append({"drafts": d, "n": torch.zeros(1, dtype=torch.int32, device=dev),
+                    "tok": torch.zeros(T_MAIN + 1, dtype=torch.int32, device=dev)})
+
+    def gumbel_part(i):
+        g = gum[i]
+        sv.spec_accept_gumbel(ctx, acc_sets[i]["logits"], g["drafts"], T_MAIN, VOCAB,
+                              GUMBEL_SEED + i, 0, g["n"], g["tok"])
+
+    for i in range(3):
+        gumbel_part(i)
+    sv.spec_sync_status(ctx)
+    g_gum = [torch.cuda.CUDAGraph() for _ in range(3)]
+    with torch.cuda.stream(side):
+        for i in range(3):
+            with torch.cuda.graph(g_gum[i], stream=side):
+                gumbel_part(i)
+    torch.cuda.synchronize()
+    KG = max(K, 30)
+    e0.record()
+    for i in range(KG):
+        g_gum[i % 3].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    gum_ms = e0.elapsed_time(e1) / KG
+    sv.spec_sync_status(ctx)
+
     # ---- 27B-class Large tier: 64 layers of per-channel int8 projections at
     # T=32 with the block-1024 random Hadamard rotation of the activations
     L8 = inputs.LAYER_27B
@@ -490,6 +530,16 @@ def run_gpu(args):
             "acceptance_ms": round(acc_ms, 5),
             "acceptance_share": round(acc_ms / (gemm_ms + acc_ms), 4),
             "accepted": accepted,
+            "accept_gumbel": {
+                "workload": "shared-seed (Gumbel-max) acceptance of the same T=32 blocks over "
+                            "V=151936: one launch reads the (T+1)xV fp32 logits once; the drafts "
+                            "are sampled on the GPU from the same q with the same seed",
+                "ms": round(gum_ms, 5),
+                "share_if_used_in_step": round(gum_ms / (gemm_ms + gum_ms), 4),
+                "logits_GB/s": round(accept_gumbel_bytes(T_MAIN) / (gum_ms * 1e-3) / 1e9, 1),
+                "accepted": [{"level": a["level"], "n_accepted": int(g["n"].item())}
+                             for a, g in zip(acc_sets, gum)],
+            },
             "t16": {
                 "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance)",
                 "ms_per_step": round(t16_ms, 5),
@@ -721,6 +771,45 @@ def run_accept_case(args):
     ctx.close()
 
 
+def run_gumbel_case(args):
+    """spec_accept_gumbel alone at T drafts over V tokens, launched warm-up +
+    steps times eagerly (for profiling the kernel in isolation); prints its
+    device time per call and the logits' read rate."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    T, V = (int(v) for v in args.gumbel_case.split(","))
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    a = inputs.accept_inputs(np.random.default_rng(11), T, V, logit_std=3.0, alpha=1.0, noise_std=0.5)
+    logits = torch.from_numpy(a.logits).to(dev)
+    logq = torch.from_numpy(np.log(a.q).astype(np.float32)).to(dev)
+    d = torch.zeros(max(T, 1), dtype=torch.int32, device=dev)
+    n = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(T + 1, dtype=torch.int32, device=dev)
+    if T > 0:
+        sv.spec_gumbel_sample(ctx, logq, T, V, GUMBEL_SEED, 0, d)
+    for _ in range(args.warmup):
+        sv.spec_accept_gumbel(ctx, logits, d, T, V, GUMBEL_SEED, 0, n, tok)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        sv.spec_accept_gumbel(ctx, logits, d, T, V, GUMBEL_SEED, 0, n, tok)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = accept_gumbel_bytes(T, V)
+    print(json.dumps({"gumbel_case": [T, V], "ms_per_call": round(ms, 6), "n_accepted": int(n.item()),
+                      "logits_GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes}),
+          flush=True)
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -734,6 +823,8 @@ def main():
                     help="host seconds the reference arm spends on warm-up + timed steps")
     ap.add_argument("--accept-case", default=None, metavar="T,V",
                     help="time spec_accept alone at T drafts over V tokens (eager launches)")
+    ap.add_argument("--gumbel-case", default=None, metavar="T,V",
+                    help="time spec_accept_gumbel alone at T drafts over V tokens (eager launches)")
     ap.add_argument("--kernel-case-w8", default=None, metavar="T,N,K[,B]",
                     help="time one per-channel int8 GEMM shape (B > 0: rotation block)")
     ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
@@ -741,6 +832,9 @@ def main():
     args = ap.parse_args()
     if args.accept_case:
         run_accept_case(args)
+        return
+    if args.gumbel_case:
+        run_gumbel_case(args)
         return
     if args.kernel_case_w8:
         run_kernel_case_w8(args)

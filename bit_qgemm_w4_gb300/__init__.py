@@ -16,7 +16,8 @@ import os
 __all__ = [
     "SpecError", "Context", "lib", "spec_create", "spec_destroy", "spec_sync_status",
     "qgemm_w4a16", "qgemm_w8a16", "fwht_rotate", "spec_softmax", "spec_accept",
-    "spec_accept_noalloc", "spec_accept_tree", "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
+    "spec_accept_noalloc", "spec_accept_tree", "spec_gumbel_sample", "spec_accept_gumbel",
+    "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
     "SPEC_DTYPE_BF16", "SPEC_DTYPE_F32",
 ]
 
@@ -28,6 +29,7 @@ SPEC_DTYPE_F32 = 1
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
+_U64 = ctypes.c_uint64
 
 # name -> argtypes (all return int status, except spec_last_error / spec_version)
 _SIGS = {
@@ -43,6 +45,8 @@ _SIGS = {
     "spec_accept": [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P],
     "spec_accept_noalloc": [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P],
     "spec_accept_tree": [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P],
+    "spec_gumbel_sample": [_P, _P, _I, _I, _U64, _U64, _P, _P, _P],
+    "spec_accept_gumbel": [_P, _P, _P, _I, _I, _U64, _U64, _P, _P, _P, _P],
     "qdequant_w4": [_P, _P, _P, _P, _I, _I, _I, _P, _P],
     "qdequant_w8": [_P, _P, _P, _I, _I, _I, _P, _P],
 }
@@ -184,6 +188,19 @@ def spec_accept_tree(ctx, target_logits, draft_tokens, parent, T, V, path_len, o
                      path_nodes, stream=None) -> None:
     _call("spec_accept_tree", _h(ctx), _ptr(target_logits), _ptr(draft_tokens), _ptr(parent), T, V,
           _ptr(path_len), _ptr(out_tokens), _ptr(path_nodes), _stream(stream))
+
+
+def spec_gumbel_sample(ctx, logits, rows, V, seed, position, out_tokens, near_tie_flags=None,
+                       stream=None) -> None:
+    _call("spec_gumbel_sample", _h(ctx), _ptr(logits), rows, V, seed % (1 << 64), position % (1 << 64),
+          _ptr(out_tokens), _ptr(near_tie_flags), _stream(stream))
+
+
+def spec_accept_gumbel(ctx, target_logits, draft_tokens, T, V, seed, position, n_accepted,
+                       out_tokens, near_tie_flags=None, stream=None) -> None:
+    _call("spec_accept_gumbel", _h(ctx), _ptr(target_logits), _ptr(draft_tokens), T, V,
+          seed % (1 << 64), position % (1 << 64), _ptr(n_accepted), _ptr(out_tokens),
+          _ptr(near_tie_flags), _stream(stream))
 
 
 def qdequant_w4(ctx, qcodes, scales, zeros, group_size, N, K, w, stream=None) -> None:

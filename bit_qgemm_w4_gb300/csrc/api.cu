@@ -98,7 +98,7 @@ namespace {
 // Workspace layout (bytes, each region 256-aligned).
 struct WsLayout {
   size_t err, counters, partials, xrot, stats, chunks, argidx, argval, acc_counters, rowstat, rowcnt,
-      total;
+      gbest, gidx, gsecond, total;
   int slots;
 };
 
@@ -122,6 +122,9 @@ WsLayout layout_for(int num_sms) {
   L.acc_counters = take(sizeof(int) * 16);
   L.rowstat = take(sizeof(double) * 2 * (size_t)4096);
   L.rowcnt = take(sizeof(int) * (size_t)4096);
+  L.gbest = take(sizeof(float) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
+  L.gidx = take(sizeof(int) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
+  L.gsecond = take(sizeof(float) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
   L.total = off;
   return L;
 }
@@ -239,6 +242,9 @@ int spec_create(int device, size_t workspace_bytes, spec_ctx** out) {
   ctx->acc_counters = reinterpret_cast<int*>(ctx->ws + L.acc_counters);
   ctx->acc_rowstat = reinterpret_cast<double*>(ctx->ws + L.rowstat);
   ctx->acc_rowcnt = reinterpret_cast<int*>(ctx->ws + L.rowcnt);
+  ctx->gum_best = reinterpret_cast<float*>(ctx->ws + L.gbest);
+  ctx->gum_idx = reinterpret_cast<int*>(ctx->ws + L.gidx);
+  ctx->gum_second = reinterpret_cast<float*>(ctx->ws + L.gsecond);
   *out = ctx;
   return SPEC_OK;
 }
@@ -392,6 +398,40 @@ int spec_accept_tree(spec_ctx* ctx, const float* target_logits, const int32_t* d
   if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
   return launch_accept_tree(ctx, target_logits, draft_tokens, parent, T, V, path_len, out_tokens,
                             path_nodes, static_cast<cudaStream_t>(stream));
+}
+
+int spec_gumbel_sample(spec_ctx* ctx, const float* logits, int rows, int V, uint64_t seed,
+                       uint64_t position, int32_t* out_tokens, int32_t* near_tie_flags, void* stream) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (rows < 1 || rows > kMaxAcceptT + 1)
+    return set_error(SPEC_ERR_SHAPE, "rows=%d outside 1..%d", rows, kMaxAcceptT + 1);
+  if (V < 1 || V > (1 << 26)) return set_error(SPEC_ERR_SHAPE, "V=%d outside 1..2^26", V);
+  SV_TRY(check_ptr(logits, 4, "logits"));
+  SV_TRY(check_ptr(out_tokens, 4, "out_tokens"));
+  if (near_tie_flags) SV_TRY(check_ptr(near_tie_flags, 4, "near_tie_flags"));
+  DeviceGuard dg(ctx->device);
+  if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
+  return launch_gumbel(ctx, logits, rows, V, seed, position, 0, nullptr, out_tokens, nullptr,
+                       near_tie_flags, static_cast<cudaStream_t>(stream));
+}
+
+int spec_accept_gumbel(spec_ctx* ctx, const float* target_logits, const int32_t* draft_tokens, int T,
+                       int V, uint64_t seed, uint64_t position, int32_t* n_accepted,
+                       int32_t* out_tokens, int32_t* near_tie_flags, void* stream) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (T < 0 || T > kMaxAcceptT) return set_error(SPEC_ERR_SHAPE, "T=%d outside 0..%d", T, kMaxAcceptT);
+  if (V < 1 || V > (1 << 26)) return set_error(SPEC_ERR_SHAPE, "V=%d outside 1..2^26", V);
+  SV_TRY(check_ptr(target_logits, 4, "target_logits"));
+  if (T > 0) SV_TRY(check_ptr(draft_tokens, 4, "draft_tokens"));
+  SV_TRY(check_ptr(n_accepted, 4, "n_accepted"));
+  SV_TRY(check_ptr(out_tokens, 4, "out_tokens"));
+  if (near_tie_flags) SV_TRY(check_ptr(near_tie_flags, 4, "near_tie_flags"));
+  DeviceGuard dg(ctx->device);
+  if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
+  return launch_gumbel(ctx, target_logits, T + 1, V, seed, position, 1, draft_tokens, out_tokens,
+                       n_accepted, near_tie_flags, static_cast<cudaStream_t>(stream));
 }
 
 int qdequant_w4(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales, const uint8_t* zeros,

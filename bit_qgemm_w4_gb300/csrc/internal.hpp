@@ -66,6 +66,9 @@ struct spec_ctx {
   int* acc_counters = nullptr;    // [16] arrival counters of the acceptance kernels
   double* acc_rowstat = nullptr;  // [4096][2] per-row (max, 1/Z) merged by row_stats
   int* acc_rowcnt = nullptr;      // [4096] per-row arrival counters of row_stats, kept zeroed
+  float* gum_best = nullptr;      // [kMaxAcceptT+1][kAcceptChunks] shared-seed sampling partials
+  int* gum_idx = nullptr;
+  float* gum_second = nullptr;
 };
 
 namespace sv {
@@ -83,6 +86,9 @@ int launch_accept_noalloc(const float* logits, const float* q, const int32_t* dr
 int launch_accept_tree(spec_ctx* ctx, const float* logits, const int32_t* drafts,
                        const int32_t* parent, int T, int V, int32_t* path_len, int32_t* tokens,
                        int32_t* nodes, cudaStream_t s);
+int launch_gumbel(spec_ctx* ctx, const float* logits, int rows, int V, uint64_t seed, uint64_t position,
+                  int accept, const int32_t* drafts, int32_t* tokens, int32_t* n_acc, int32_t* flags,
+                  cudaStream_t s);
 int launch_dequant(spec_ctx* ctx, int quant, const void* qcodes, const uint16_t* scales,
                    const uint8_t* zeros, int group_size, int N, int K, float* w, cudaStream_t s);
 }  // namespace sv

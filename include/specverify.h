@@ -92,8 +92,8 @@ int spec_destroy(spec_ctx* ctx);
 /* Synchronise `stream`, then read and clear the context's device error word.
  * Returns SPEC_OK or the first device-side error recorded since the last call:
  * SPEC_ERR_TIMEOUT when a bounded wait ran out, SPEC_ERR_ARG when a draft token
- * (spec_accept) or parent index (spec_accept_tree) read on the device was out
- * of range (that draft/node was treated as rejected).  After an error the
+ * (spec_accept, spec_accept_gumbel) or parent index (spec_accept_tree) read on
+ * the device was out of range (that draft/node was treated as rejected).  After an error the
  * split-K counters and partial sums are re-zeroed so the context is usable
  * again. */
 int spec_sync_status(spec_ctx* ctx, void* stream);
@@ -216,6 +216,47 @@ int spec_accept_tree(spec_ctx* ctx, const float* target_logits,
                      const int32_t* draft_tokens, const int32_t* parent, int T,
                      int V, int32_t* path_len, int32_t* out_tokens,
                      int32_t* path_nodes, void* stream);
+
+/* Shared-seed sampling and acceptance (the trymirai post feed, the post with
+ * the "random number from 1 to 10" example: sample the speculator and the
+ * LLM with the same seed through the Gumbel-max trick, so that matching
+ * distributions give matching tokens).
+ *
+ * Noise: the uniform of token v at draft position p is word v mod 4 of
+ * Philox4x32-10 (Salmon et al., SC 2011) at counter (v div 4, p mod 2^32,
+ * p div 2^32, 0) under key (seed mod 2^32, seed div 2^32), a word w giving
+ * u = (2 floor(w / 2^9) + 1) / 2^24.  The sample of a row is
+ * argmax_v (logit_v - log(-log u_v)), computed in fp32, equal values to the
+ * smallest token id.  A row's near-tie flag is 1 when its best value exceeds
+ * every other token's by less than 1e-4 (another summation order could pick
+ * the runner-up there).
+ *
+ * spec_gumbel_sample: the drafter's side.
+ *   logits fp32 [rows][V] (device), row r sampled at position + r.
+ *   out_tokens int32 [rows]; near_tie_flags nullable int32 [rows] (device).
+ *   1 <= rows <= 257, 1 <= V <= 2^26.  Pointers need 4-byte alignment.
+ *
+ * spec_accept_gumbel: the verifier's side.
+ *   target_logits fp32 [T+1][V]: row i scores draft position i, row T follows
+ *                 the last draft; row i is sampled at position + i.
+ *   draft_tokens  int32 [T] (nullable when T = 0), drawn by the speculator
+ *                 under the same seed and positions.
+ * Drafts are accepted left to right while each equals the target's sample at
+ * its position; the first position that differs, or position T, emits the
+ * target's sample.  Outputs (device): n_accepted int32 [1]; out_tokens int32
+ * [T+1], the first n_accepted + 1 valid; near_tie_flags nullable int32 [T+1].
+ * A draft outside [0, V) never matches and is reported by spec_sync_status.
+ * 0 <= T <= 256, 1 <= V <= 2^26.  One launch; the context's sampling
+ * partials are shared by both entries, so keep calls on one context ordered
+ * on one stream. */
+int spec_gumbel_sample(spec_ctx* ctx, const float* logits, int rows, int V,
+                       uint64_t seed, uint64_t position, int32_t* out_tokens,
+                       int32_t* near_tie_flags, void* stream);
+int spec_accept_gumbel(spec_ctx* ctx, const float* target_logits,
+                       const int32_t* draft_tokens, int T, int V, uint64_t seed,
+                       uint64_t position, int32_t* n_accepted,
+                       int32_t* out_tokens, int32_t* near_tie_flags,
+                       void* stream);
 
 /* Dequantised weights as fp32 [N][K] (exact: (code - zero) * scale and
  * code * scale both fit in fp32), for checking a packed checkpoint.  Layouts

@@ -68,9 +68,21 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// g = -log(e), e = -log(u).  e needs a small relative error, which the fast
+// logarithm (absolute error a few 1e-7 near 1) lacks as u -> 1; there
+// e = -log(1 - d) = d + d^2/2 + d^3/3 + ... with d = 1 - u, exact from the
+// same integer, truncated after d^6 (relative error below d^6 / 7 < 1e-8 for
+// d < 1/16).  The outer logarithm only needs a small absolute error: the
+// fast one keeps g within a few 1e-6 of the exact value, far inside the
+// 1e-4 near-tie band.
 __device__ __forceinline__ float gumbel_of(uint32_t w) {
-  const float u = (float)(2u * (w >> 9) + 1u) * 0x1p-24f;
-  return -logf(-logf(u));
+  const uint32_t m = w >> 9;                                  // u = (2m + 1) / 2^24
+  const float u = (float)(2u * m + 1u) * 0x1p-24f;
+  const float d = (float)(2u * (0x7FFFFFu - m) + 1u) * 0x1p-24f;   // 1 - u
+  const float series =
+      d * (1.f + d * (0.5f + d * (1.f / 3.f + d * (0.25f + d * (0.2f + d * (1.f / 6.f))))));
+  const float e = u > 0.9375f ? series : -__logf(u);
+  return -__logf(e);
 }
 
 // The best (value, token) of a set and the largest value of the rest.
@@ -105,8 +117,9 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
 
 __global__ void __launch_bounds__(kGBlock) gumbel_kernel(GumbelArgs a) {
   __shared__ Top2 sh[kGBlock / 32];
-  __shared__ int s_last;
+  __shared__ int s_last, s_n;
   __shared__ int s_tok[kMaxAcceptT + 1];
+  __shared__ int s_draft[kMaxAcceptT];
 
   const int c = blockIdx.x, row = blockIdx.y;
   const int lo = c * a.chunk;
@@ -153,41 +166,48 @@ __global__ void __launch_bounds__(kGBlock) gumbel_kernel(GumbelArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // last block: every row's token, then the drafts
-  for (int r = threadIdx.x; r < a.rows; r += kGBlock) {
+  // last block: one warp per row merges the row's chunks (lanes over chunks)
+  for (int r = warp; r < a.rows; r += kGBlock / 32) {
     Top2 m{-INFINITY, kNoToken, -INFINITY};
-    for (int k = 0; k < a.nchunks; ++k) {
+    for (int k = lane; k < a.nchunks; k += 32) {
       const int at = r * a.nchunks + k;
       m = top2_merge(m, Top2{__ldcg(a.best + at), __ldcg(a.idx + at), __ldcg(a.second + at)});
     }
-    const int tok = m.i == kNoToken ? 0 : m.i;   // a row of NaNs: token 0
-    s_tok[r] = tok;
-    if (a.flags) a.flags[r] = (m.b - m.s < kGTieEps) ? 1 : 0;
-    if (!a.accept) a.tokens[r] = tok;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const Top2 u{__shfl_xor_sync(0xffffffffu, m.b, o), __shfl_xor_sync(0xffffffffu, m.i, o),
+                   __shfl_xor_sync(0xffffffffu, m.s, o)};
+      m = top2_merge(m, u);
+    }
+    if (lane == 0) {
+      const int tok = m.i == kNoToken ? 0 : m.i;   // a row of NaNs: token 0
+      s_tok[r] = tok;
+      if (a.flags) a.flags[r] = (m.b - m.s < kGTieEps) ? 1 : 0;
+      if (!a.accept) a.tokens[r] = tok;
+    }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    if (a.accept) {
-      const int T = a.rows - 1;
-      int n = T;
-      for (int i = 0; i < T; ++i) {
-        const int d = a.drafts[i];
-        if (d < 0 || d >= a.V) {   // never matches; reported
-          atomicCAS(a.err, 0, kDevErrBadToken);
-          n = i;
-          break;
-        }
-        if (d != s_tok[i]) {
-          n = i;
-          break;
-        }
-      }
-      for (int i = 0; i < n; ++i) a.tokens[i] = a.drafts[i];
+  if (a.accept) {
+    // every draft tested at once; the first rejection is the smallest
+    // failing position
+    const int T = a.rows - 1;
+    if (threadIdx.x == 0) s_n = T;
+    __syncthreads();
+    for (int i = threadIdx.x; i < T; i += kGBlock) {
+      const int d = a.drafts[i];
+      s_draft[i] = d;
+      if (d < 0 || d >= a.V || d != s_tok[i]) atomicMin(&s_n, i);
+    }
+    __syncthreads();
+    const int n = s_n;
+    for (int i = threadIdx.x; i < n; i += kGBlock) a.tokens[i] = s_draft[i];
+    if (threadIdx.x == 0) {
+      if (n < T && (s_draft[n] < 0 || s_draft[n] >= a.V))   // never matches; reported
+        atomicCAS(a.err, 0, kDevErrBadToken);
       a.tokens[n] = s_tok[n];
       *a.n_acc = n;
     }
-    *a.counter = 0;
   }
+  if (threadIdx.x == 0) *a.counter = 0;
 }
 
 }  // namespace
@@ -199,8 +219,15 @@ int launch_gumbel(spec_ctx* ctx, const float* logits, int rows, int V, uint64_t 
   a.logits = logits;
   a.rows = rows;
   a.V = V;
-  // about four blocks per SM in all, at least 1024 tokens a block
-  long long want = (4LL * ctx->num_sms + rows - 1) / rows;
+  // one full wave of resident blocks in all, at least 1024 tokens a block
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gumbel_kernel, kGBlock, 0) != cudaSuccess || b < 1)
+      b = 4;
+    per_sm = b;
+  }
+  long long want = (long long)per_sm * ctx->num_sms / rows;
   long long by_size = ((long long)V + 1023) / 1024;
   long long nc = want < by_size ? want : by_size;
   if (nc < 1) nc = 1;

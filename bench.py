@@ -406,6 +406,42 @@ def run_gpu(args):
     gum_ms = e0.elapsed_time(e1) / KG
     sv.spec_sync_status(ctx)
 
+    # ---- greedy tree acceptance: 4 branches x depth 8 (T=32) and 8 x 8
+    # (T=64) over V=151936, drafts matching the row argmax with p = 0.7
+    tree_res = []
+    for Tt in (32, 64):
+        tin = inputs.tree_inputs(np.random.default_rng(500 + Tt), Tt, VOCAB, logit_std=3.0, p_match=0.7)
+        tbuf = {"l": torch.from_numpy(tin.logits).to(dev), "d": torch.from_numpy(tin.drafts).to(dev),
+                "p": torch.from_numpy(tin.parent).to(dev),
+                "n": torch.zeros(1, dtype=torch.int32, device=dev),
+                "t": torch.zeros(Tt + 1, dtype=torch.int32, device=dev),
+                "k": torch.zeros(Tt, dtype=torch.int32, device=dev)}
+
+        def tree_call(b=tbuf, T_=Tt):
+            sv.spec_accept_tree(ctx, b["l"], b["d"], b["p"], T_, VOCAB, b["n"], b["t"], b["k"])
+
+        tree_call()
+        sv.spec_sync_status(ctx)
+        g_tree = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g_tree, stream=side):
+                tree_call()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g_tree.replay()
+        KT = max(K, 30)
+        e0.record()
+        for _ in range(KT):
+            g_tree.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        t_ms = e0.elapsed_time(e1) / KT
+        sv.spec_sync_status(ctx)
+        tree_res.append({"T": Tt, "branches": max(1, Tt // 8), "depth": min(Tt, 8), "ms": round(t_ms, 5),
+                         "logits_GB/s": round((Tt + 1) * VOCAB * 4 / (t_ms * 1e-3) / 1e9, 1),
+                         "path_len": int(tbuf["n"].item())})
+        del tbuf, g_tree
+
     # ---- 27B-class Large tier: 64 layers of per-channel int8 projections at
     # T=32 with the block-1024 random Hadamard rotation of the activations
     L8 = inputs.LAYER_27B
@@ -539,6 +575,11 @@ def run_gpu(args):
                 "logits_GB/s": round(accept_gumbel_bytes(T_MAIN) / (gum_ms * 1e-3) / 1e9, 1),
                 "accepted": [{"level": a["level"], "n_accepted": int(g["n"].item())}
                              for a, g in zip(acc_sets, gum)],
+            },
+            "accept_tree": {
+                "workload": "greedy tree acceptance over V=151936 (one launch; reads the (T+1)xV "
+                            "fp32 logits once)",
+                "cases": tree_res,
             },
             "t16": {
                 "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance)",
@@ -810,6 +851,44 @@ def run_gumbel_case(args):
     ctx.close()
 
 
+def run_tree_case(args):
+    """spec_accept_tree alone on a tree of T nodes over V tokens, launched
+    warm-up + steps times eagerly (for profiling); prints its device time per
+    call and the logits' read rate."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    T, V = (int(v) for v in args.tree_case.split(","))
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    tin = inputs.tree_inputs(np.random.default_rng(500 + T), T, V, logit_std=3.0, p_match=0.7)
+    logits = torch.from_numpy(tin.logits).to(dev)
+    d = torch.from_numpy(tin.drafts).to(dev)
+    par = torch.from_numpy(tin.parent).to(dev)
+    n = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(T + 1, dtype=torch.int32, device=dev)
+    nodes = torch.zeros(T, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        sv.spec_accept_tree(ctx, logits, d, par, T, V, n, tok, nodes)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        sv.spec_accept_tree(ctx, logits, d, par, T, V, n, tok, nodes)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = (T + 1) * V * 4
+    print(json.dumps({"tree_case": [T, V], "ms_per_call": round(ms, 6), "path_len": int(n.item()),
+                      "logits_GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "logits_bytes": nbytes}),
+          flush=True)
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -823,6 +902,8 @@ def main():
                     help="host seconds the reference arm spends on warm-up + timed steps")
     ap.add_argument("--accept-case", default=None, metavar="T,V",
                     help="time spec_accept alone at T drafts over V tokens (eager launches)")
+    ap.add_argument("--tree-case", default=None, metavar="T,V",
+                    help="time spec_accept_tree alone on a T-node tree over V tokens (eager launches)")
     ap.add_argument("--gumbel-case", default=None, metavar="T,V",
                     help="time spec_accept_gumbel alone at T drafts over V tokens (eager launches)")
     ap.add_argument("--kernel-case-w8", default=None, metavar="T,N,K[,B]",
@@ -835,6 +916,9 @@ def main():
         return
     if args.gumbel_case:
         run_gumbel_case(args)
+        return
+    if args.tree_case:
+        run_tree_case(args)
         return
     if args.kernel_case_w8:
         run_kernel_case_w8(args)

@@ -33,6 +33,7 @@ namespace sv {
 namespace {
 
 constexpr int kBlock = 256;
+constexpr int kMergeBatch = 1024;   // chunk partials staged in shared memory at a time
 constexpr int kDevErrBadToken = 2;
 constexpr int kDevErrBadParent = 3;
 constexpr double kTieEps = 1e-4;   // |u - p/q| band reported as a near tie
@@ -404,6 +405,8 @@ struct TreeArgs {
   const int32_t* drafts;
   const int32_t* parent;
   int T, V, nchunks;
+  int chunk;             // tokens per block, a multiple of 4
+  int vec;               // rows start on 16-byte boundaries
   float* argval;         // [T+1][nchunks]
   int* argidx;
   int* counter;
@@ -424,18 +427,38 @@ __global__ void __launch_bounds__(kBlock) tree_kernel(TreeArgs a) {
   __shared__ int amax[kMaxAcceptT + 1];
   __shared__ int depth[kMaxAcceptT];
   __shared__ unsigned char ok[kMaxAcceptT];
+  __shared__ int s_draft[kMaxAcceptT];
+  __shared__ int s_par[kMaxAcceptT];
+  __shared__ float s_mv[kMergeBatch];
+  __shared__ int s_mi[kMergeBatch];
 
   const int c = blockIdx.x, row = blockIdx.y;
-  int lo, hi;
-  chunk_range(c, a.nchunks, a.V, lo, hi);
+  const int lo = c * a.chunk;
+  const int hi = min(a.V, lo + a.chunk);
   const float* l = a.logits + (long long)row * a.V;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
-  for (int v = lo + threadIdx.x; v < hi; v += kBlock) {
-    const float x = __ldg(l + v);
-    if (better(x, v, bv, bi)) {
-      bv = x;
-      bi = v;
+  // four tokens per thread and step, 16-byte loads when the rows are
+  // aligned, unrolled so that several loads are in flight per thread
+#pragma unroll 4
+  for (int v0 = lo + 4 * threadIdx.x; v0 < hi; v0 += 4 * kBlock) {
+    float x[4];
+    if (a.vec && v0 + 3 < hi) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(l + v0));
+      x[0] = f.x;
+      x[1] = f.y;
+      x[2] = f.z;
+      x[3] = f.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = v0 + j < hi ? __ldg(l + v0 + j) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (v0 + j < hi && better(x[j], v0 + j, bv, bi)) {
+        bv = x[j];
+        bi = v0 + j;
+      }
     }
   }
 #pragma unroll
@@ -469,24 +492,50 @@ __global__ void __launch_bounds__(kBlock) tree_kernel(TreeArgs a) {
   if (!s_last) return;
   __threadfence();
   const int T = a.T;
-  for (int r = threadIdx.x; r <= T; r += kBlock) {
-    float v = -INFINITY;
-    int idx = 0x7fffffff;
-    for (int k = 0; k < a.nchunks; ++k) {
-      const float cv = __ldcg(a.argval + r * a.nchunks + k);
-      const int ci = __ldcg(a.argidx + r * a.nchunks + k);
-      if (better(cv, ci, v, idx)) {
-        v = cv;
-        idx = ci;
-      }
-    }
-    amax[r] = idx == 0x7fffffff ? 0 : idx;   // all-NaN row: token 0
+  // the drafts and parents into shared memory at once; the chunk partials
+  // in batches of rows, every load of a batch in flight together, then one
+  // warp per row merges the row's chunks from shared memory
+  for (int i = threadIdx.x; i < T; i += kBlock) {
+    s_draft[i] = a.drafts[i];
+    s_par[i] = a.parent[i];
   }
-  __syncthreads();
+  const int nc = a.nchunks;
+  const int batch_rows = kMergeBatch / nc;
+  for (int r0 = 0; r0 <= T; r0 += batch_rows) {
+    const int r1 = min(T + 1, r0 + batch_rows);
+    for (int e = threadIdx.x; e < (r1 - r0) * nc; e += kBlock) {
+      s_mv[e] = __ldcg(a.argval + r0 * nc + e);
+      s_mi[e] = __ldcg(a.argidx + r0 * nc + e);
+    }
+    __syncthreads();
+    for (int r = r0 + warp; r < r1; r += kBlock / 32) {
+      float v = -INFINITY;
+      int idx = 0x7fffffff;
+      for (int k = lane; k < nc; k += 32) {
+        const float cv = s_mv[(r - r0) * nc + k];
+        const int ci = s_mi[(r - r0) * nc + k];
+        if (better(cv, ci, v, idx)) {
+          v = cv;
+          idx = ci;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (better(ov, oi, v, idx)) {
+          v = ov;
+          idx = oi;
+        }
+      }
+      if (lane == 0) amax[r] = idx == 0x7fffffff ? 0 : idx;   // all-NaN row: token 0
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     int best = -1;
     for (int i = 0; i < T; ++i) {
-      int par = a.parent[i];
+      int par = s_par[i];
       int row_i, d;
       bool pok;
       if (par < -1 || par >= i) {   // not a topological parent: node rejected, reported
@@ -504,7 +553,7 @@ __global__ void __launch_bounds__(kBlock) tree_kernel(TreeArgs a) {
         row_i = par + 1;
         d = depth[par] + 1;
       }
-      ok[i] = (pok && a.drafts[i] == amax[row_i]) ? 1 : 0;
+      ok[i] = (pok && s_draft[i] == amax[row_i]) ? 1 : 0;
       depth[i] = d;
       if (ok[i] && (best < 0 || d > depth[best])) best = i;
     }
@@ -512,8 +561,8 @@ __global__ void __launch_bounds__(kBlock) tree_kernel(TreeArgs a) {
     int n = best;
     for (int k = len - 1; k >= 0; --k) {
       a.nodes[k] = n;
-      a.tokens[k] = a.drafts[n];
-      n = a.parent[n];
+      a.tokens[k] = s_draft[n];
+      n = s_par[n];
     }
     a.tokens[len] = amax[best + 1];
     a.path_len[0] = len;
@@ -584,7 +633,22 @@ int launch_accept_tree(spec_ctx* ctx, const float* logits, const int32_t* drafts
   a.parent = parent;
   a.T = T;
   a.V = V;
-  a.nchunks = stat_chunks(ctx, rows, V);
+  // one full wave of resident blocks in all, at least 1024 tokens a block
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tree_kernel, kBlock, 0) != cudaSuccess || b < 1) b = 4;
+    per_sm = b;
+  }
+  long long want = (long long)per_sm * ctx->num_sms / rows;
+  long long by_size = ((long long)V + 1023) / 1024;
+  long long nc = want < by_size ? want : by_size;
+  if (nc < 1) nc = 1;
+  if (nc > kAcceptChunks) nc = kAcceptChunks;
+  const long long chunk = (((long long)V + nc - 1) / nc + 3) / 4 * 4;
+  a.chunk = (int)chunk;
+  a.nchunks = (int)(((long long)V + chunk - 1) / chunk);
+  a.vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
   a.argval = ctx->acc_argval;
   a.argidx = ctx->acc_argmax;
   a.counter = ctx->acc_counters + 1;

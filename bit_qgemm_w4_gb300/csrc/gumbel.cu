@@ -34,6 +34,7 @@ constexpr int kGBlock = 256;
 constexpr float kGTieEps = 1e-4f;   // best minus runner-up below this: a near tie
 constexpr int kDevErrBadToken = 2;
 constexpr int kNoToken = 0x7fffffff;
+constexpr int kMergeBatch = 1024;   // chunk partials staged in shared memory at a time
 
 struct GumbelArgs {
   const float* logits;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kGBlock) gumbel_kernel(GumbelArgs a) {
   __shared__ int s_last, s_n;
   __shared__ int s_tok[kMaxAcceptT + 1];
   __shared__ int s_draft[kMaxAcceptT];
+  __shared__ Top2 s_part[kMergeBatch];
 
   const int c = blockIdx.x, row = blockIdx.y;
   const int lo = c * a.chunk;
@@ -166,25 +168,35 @@ __global__ void __launch_bounds__(kGBlock) gumbel_kernel(GumbelArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // last block: one warp per row merges the row's chunks (lanes over chunks)
-  for (int r = warp; r < a.rows; r += kGBlock / 32) {
-    Top2 m{-INFINITY, kNoToken, -INFINITY};
-    for (int k = lane; k < a.nchunks; k += 32) {
-      const int at = r * a.nchunks + k;
-      m = top2_merge(m, Top2{__ldcg(a.best + at), __ldcg(a.idx + at), __ldcg(a.second + at)});
+  // last block: the chunk partials in batches of rows, every load of a
+  // batch in flight together, then one warp per row merges the row's chunks
+  // from shared memory (lanes over chunks)
+  const int nc = a.nchunks;
+  const int batch_rows = kMergeBatch / nc;
+  for (int r0 = 0; r0 < a.rows; r0 += batch_rows) {
+    const int r1 = min(a.rows, r0 + batch_rows);
+    for (int e = threadIdx.x; e < (r1 - r0) * nc; e += kGBlock) {
+      const int at = r0 * nc + e;
+      s_part[e] = Top2{__ldcg(a.best + at), __ldcg(a.idx + at), __ldcg(a.second + at)};
     }
+    __syncthreads();
+    for (int r = r0 + warp; r < r1; r += kGBlock / 32) {
+      Top2 m{-INFINITY, kNoToken, -INFINITY};
+      for (int k = lane; k < nc; k += 32) m = top2_merge(m, s_part[(r - r0) * nc + k]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const Top2 u{__shfl_xor_sync(0xffffffffu, m.b, o), __shfl_xor_sync(0xffffffffu, m.i, o),
-                   __shfl_xor_sync(0xffffffffu, m.s, o)};
-      m = top2_merge(m, u);
+      for (int o = 16; o > 0; o >>= 1) {
+        const Top2 u{__shfl_xor_sync(0xffffffffu, m.b, o), __shfl_xor_sync(0xffffffffu, m.i, o),
+                     __shfl_xor_sync(0xffffffffu, m.s, o)};
+        m = top2_merge(m, u);
+      }
+      if (lane == 0) {
+        const int tok = m.i == kNoToken ? 0 : m.i;   // a row of NaNs: token 0
+        s_tok[r] = tok;
+        if (a.flags) a.flags[r] = (m.b - m.s < kGTieEps) ? 1 : 0;
+        if (!a.accept) a.tokens[r] = tok;
+      }
     }
-    if (lane == 0) {
-      const int tok = m.i == kNoToken ? 0 : m.i;   // a row of NaNs: token 0
-      s_tok[r] = tok;
-      if (a.flags) a.flags[r] = (m.b - m.s < kGTieEps) ? 1 : 0;
-      if (!a.accept) a.tokens[r] = tok;
-    }
+    __syncthreads();
   }
   if (a.accept) {
     // every draft tested at once; the first rejection is the smallest

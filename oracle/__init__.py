@@ -33,7 +33,7 @@ argmax) standing in for a step where the definition is plain.  Sources:
   easy as 1, 2, 3", SC 2011), a counter-based generator that the CUDA path
   implements separately from the same published definition.
 
-Readings where the sources are silent (each is listed in the design doc):
+Readings where the sources are silent:
 dequantisation w = (code - zero) * scale with groups of g consecutive k
 inside one output row; Sylvester (natural-order) Hadamard with 1/sqrt(B);
 T+1 uniforms (u[0..T-1] for the accept tests, u[T] for the one final draw);

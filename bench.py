@@ -277,9 +277,20 @@ def run_gpu(args):
     layers = [[inputs.w4_weights_device(gen, N, K, dev, GROUP) for _, K, N in inputs.LAYER_9B]
               for _ in range(inputs.LAYERS_9B)]
     head = inputs.w4_weights_device(gen, VOCAB, HIDDEN, dev, GROUP)
-    xs = [[inputs.activations_device(gen, T_MAIN, K, dev) for _, K, _ in inputs.LAYER_9B]
-          for _ in range(inputs.LAYERS_9B)]
-    x_head = inputs.activations_device(gen, T_MAIN, HIDDEN, dev)
+    # every activation of a step lives in one device buffer (views per GEMM),
+    # so the end-to-end run stages a step's activations with one copy
+    x_elems = inputs.LAYERS_9B * sum(T_MAIN * K for _, K, _ in inputs.LAYER_9B) + T_MAIN * HIDDEN
+    x_flat = torch.empty(x_elems, dtype=torch.bfloat16, device=dev)
+    x_off = [0]
+
+    def x_view(K):
+        v = x_flat[x_off[0]:x_off[0] + T_MAIN * K].view(T_MAIN, K)
+        x_off[0] += T_MAIN * K
+        v.copy_(inputs.activations_device(gen, T_MAIN, K, dev))
+        return v
+
+    xs = [[x_view(K) for _, K, _ in inputs.LAYER_9B] for _ in range(inputs.LAYERS_9B)]
+    x_head = x_view(HIDDEN)
     ys = [torch.empty((T_MAIN, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_9B]
     logits_head = torch.empty((T_MAIN, VOCAB), dtype=torch.float32, device=dev)
 
@@ -482,13 +493,11 @@ def run_gpu(args):
     # ---- end to end: inputs copied from pinned host memory every step,
     # result (accepted count + tokens) read back every step
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
-    h_x = [[pin(xs[l][j]) for j in range(len(inputs.LAYER_9B))] for l in range(inputs.LAYERS_9B)]
-    h_xh = pin(x_head)
+    h_xflat = pin(x_flat)
     h_acc = [{k: pin(a[k]) for k in ("logits", "q", "drafts", "u")} for a in acc_sets]
     h_out = [torch.empty(1, dtype=torch.int32).pin_memory(),
              torch.empty(T_MAIN + 1, dtype=torch.int32).pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for row in h_x for t in row) + \
-        h_xh.numel() * h_xh.element_size() + \
+    h2d = h_xflat.numel() * h_xflat.element_size() + \
         sum(v.numel() * v.element_size() for v in h_acc[0].values())
     d2h = 4 * (T_MAIN + 2)
     K_e2e = max(10, min(K, 200))
@@ -497,10 +506,7 @@ def run_gpu(args):
     dist_barrier(world)
     e2e_evs[0].record()
     for i in range(K_e2e):
-        for l in range(inputs.LAYERS_9B):
-            for j in range(len(inputs.LAYER_9B)):
-                xs[l][j].copy_(h_x[l][j], non_blocking=True)
-        x_head.copy_(h_xh, non_blocking=True)
+        x_flat.copy_(h_xflat, non_blocking=True)
         a, ha = acc_sets[i % 3], h_acc[i % 3]
         for k in ("logits", "q", "drafts", "u"):
             a[k].copy_(ha[k], non_blocking=True)

@@ -12,9 +12,14 @@ generator; they exceed L2, so no step reuses another's cached weights.
 
 Printed: one JSON line.  `value` is algorithmic HBM bytes per step / device
 time per step (GB/s) with inputs resident; `e2e` is the same metric when
-every step also copies its inputs from pinned host memory and reads its
-result back; `t16` is the same stack at T = 16 without head and acceptance.
-`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+every step also copies its inputs from pinned host memory (double-buffered
+against the previous step's compute) and reads its result back.  Sub-objects
+time, each on its own graph: `t16` (the stack at T = 16 without head and
+acceptance), `w8_27b` (the 27B-class int8 stack with rotation),
+`accept_gumbel` (shared-seed acceptance of the same blocks) and `accept_tree`
+(greedy trees of 32 and 64 nodes).  `--impl reference` times the fp64 CPU
+oracle on a bounded sample instead; `--kernel-case`, `--kernel-case-w8`,
+`--accept-case`, `--gumbel-case` and `--tree-case` time one kernel alone.
 """
 from __future__ import annotations
 

@@ -207,6 +207,12 @@ def dist_barrier(world):
         dist.barrier()
 
 
+def whole_job_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank processes one
+    step's bytes per step, and a step takes the slowest rank's time."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_max(world, value: float, device=None) -> float:
     if world == 1:
         return value
@@ -619,7 +625,7 @@ def run_gpu(args):
     if rank == 0:
         out = {
             "metric": METRIC,
-            "value": round(world * nbytes / (ms_per_step * 1e-3) / 1e9, 2),
+            "value": round(whole_job_gbs(world, nbytes, ms_per_step), 2),
             "unit": "GB/s",
             "n_gpus": world,
             "steps": K,
@@ -692,7 +698,7 @@ def run_gpu(args):
             },
             "cpu_baseline": cpu,
             "e2e": {
-                "value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "value": round(whole_job_gbs(world, nbytes, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "steps": K_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "staging": "double-buffered device inputs: step i+1's host-to-device copy runs on a "

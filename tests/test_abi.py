@@ -46,3 +46,42 @@ def test_null_context_is_rejected_without_touching_a_gpu(lib):
 
 def test_create_out_pointer_checked(lib):
     assert lib.spec_create(0, 0, None) == -1
+
+
+def _declared_params():
+    """(name, [parameter declarations]) for every function in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+        params = [p.strip() for p in m.group(2).replace("\n", " ").split(",")]
+        out[m.group(1)] = [p for p in params if p and p != "void"]
+    return out
+
+
+def _kind_of_param(decl: str) -> str:
+    if "*" in decl:
+        return "pointer"
+    if decl.startswith(("uint64_t", "size_t")):
+        return "u64"
+    if decl.startswith("int"):
+        return "i32"
+    raise AssertionError(f"unexpected parameter type: {decl}")
+
+
+def _kind_of_ctype(t) -> str:
+    if t is ctypes.c_void_p or getattr(t, "_type_", None) is ctypes.c_void_p:
+        return "pointer"
+    if ctypes.sizeof(t) == 8:
+        return "u64"
+    if ctypes.sizeof(t) == 4:
+        return "i32"
+    raise AssertionError(f"unexpected ctype: {t}")
+
+
+def test_binding_argument_lists_match_the_header():
+    # a missing or mistyped argument would pass garbage through the C ABI
+    decl = _declared_params()
+    for name, argtypes in sv._SIGS.items():
+        want = [_kind_of_param(p) for p in decl[name]]
+        got = [_kind_of_ctype(t) for t in argtypes]
+        assert got == want, (name, got, want)

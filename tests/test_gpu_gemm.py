@@ -178,25 +178,30 @@ def _sample_pairs(rng, N, n_pairs=64):
 
 
 @pytest.mark.parametrize("T,N,K", [(16, 6144, 4096), (32, 24576, 4096), (16, 4096, 12288),
-                                   (32, 151936, 4096)])
-def test_w4_full_size_sampled(ctx, T, N, K):
+                                   (32, 4096, 12288), (32, 151936, 4096)])
+@pytest.mark.parametrize("f32", [True, False])
+def test_w4_full_size_sampled(ctx, T, N, K, f32):
     rng = np.random.default_rng(4000 + N + T)
     W = inputs.w4_weights(rng, N, K, 64, keep_raw=False)
     xb = inputs.activations(rng, T, K)
-    y = _run_w4(ctx, W, xb, T, False)
+    y = _run_w4(ctx, W, xb, T, f32)
     rows = _sample_pairs(rng, N)
     S = _w4_rows(W, rows)
     ref = oracle.qgemm_w4a16(S.qcodes, S.scales, S.zeros, 64, xb, T, len(rows), K)
-    assert gemm_error_ratio(y[:, rows], ref, True) <= 1.0
+    assert gemm_error_ratio(y[:, rows], ref, not f32) <= 1.0
 
 
-def test_w8_rotated_full_size_sampled(ctx):
-    rng = np.random.default_rng(4500)
-    T, N, K, B = 32, 34816, 5120, 1024
+@pytest.mark.parametrize("N,K", [(34816, 5120), (5120, 17408)])
+@pytest.mark.parametrize("f32", [True, False])
+def test_w8_rotated_full_size_sampled(ctx, N, K, f32):
+    # the 27B-class gate_up (K = 5 rotation blocks) and down projection
+    # (K = 17408 = 17 blocks of 1024, the only odd block count)
+    rng = np.random.default_rng(4500 + K)
+    T, B = 32, 1024
     W = inputs.w8_weights(rng, N, K, 0)
     xb = inputs.activations(rng, T, K)
     s = inputs.hadamard_signs(rng, K)
-    y = _run_w8(ctx, W, xb, T, False, s, B)
+    y = _run_w8(ctx, W, xb, T, f32, s, B)
     rows = np.sort(rng.choice(N, size=128, replace=False))
     ref = oracle.qgemm_w8a16(W.qcodes[rows], W.scales[rows], 0, xb, T, len(rows), K, s, B)
-    assert gemm_error_ratio(y[:, rows], ref, True) <= 1.0
+    assert gemm_error_ratio(y[:, rows], ref, not f32) <= 1.0

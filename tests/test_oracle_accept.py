@@ -151,7 +151,7 @@ def test_distribution_preserved_chi_square():
     q = scipy.special.softmax(rng.standard_normal((2, V)) * 1.5, axis=-1)
     # store p through float32 logits as the oracle reads them
     p = scipy.special.softmax(np.log(p).astype(np.float32).astype(np.float64), axis=-1)
-    n_trials = 200_000
+    n_trials = 1_000_000
     out = _chain_trials(p, q, n_trials, seed=11)
     crit = scipy.stats.chi2.ppf(0.999, V - 1)   # 24.32
     obs0 = np.bincount(out[:, 0], minlength=V)

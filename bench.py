@@ -92,10 +92,6 @@ def step_bytes(T: int = T_MAIN) -> int:
     return stack_bytes(T) + head_bytes(T) + accept_bytes(T)
 
 
-def gemm_launches_per_step() -> int:
-    return inputs.LAYERS_9B * len(inputs.LAYER_9B) + 1
-
-
 # ----------------------------------------------------------------------------
 # peaks, clocks, ncu traffic
 # ----------------------------------------------------------------------------
@@ -227,29 +223,6 @@ def dist_max(world, value: float, device=None) -> float:
 # CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(layer_host, x_host, acc_host, budget_s: float = 12.0):
-    """Time the fp64 oracle on a bounded sample of the step: layer 0's GEMMs
-    in order until the time budget is spent (at least one), then the
-    acceptance rule on one sweep point.  Returns (GB/s, seconds, description)."""
-    import oracle
-    t0 = time.perf_counter()
-    done_bytes = 0
-    names = []
-    for (name, K, N), w, xb in zip(inputs.LAYER_9B, layer_host, x_host):
-        oracle.qgemm_w4a16(w["qcodes"], w["scales"], w["zeros"], GROUP, xb, T_MAIN, N, K)
-        done_bytes += w4_gemm_bytes(T_MAIN, N, K)
-        names.append(name)
-        if time.perf_counter() - t0 > budget_s:
-            break
-    a = acc_host
-    oracle.spec_accept(a.logits, a.q, a.drafts, a.u)
-    done_bytes += accept_bytes(T_MAIN)
-    dt = time.perf_counter() - t0
-    desc = (f"oracle (numpy fp64) on layer 0 {'+'.join(names)} at T=32 and one spec_accept "
-            f"over V={VOCAB}: {done_bytes / 1e6:.0f} MB of the step's {step_bytes() / 1e9:.2f} GB")
-    return done_bytes / dt / 1e9, dt, desc
-
-
 def host_layer0(seed: int = 4242):
     """Layer-0 weights, activations and one acceptance input set on the host
     (numpy generators; value distributions as the device stack)."""
@@ -292,16 +265,24 @@ def run_gpu(args):
     # so the end-to-end run stages a step's activations with one copy
     x_elems = inputs.LAYERS_9B * sum(T_MAIN * K for _, K, _ in inputs.LAYER_9B) + T_MAIN * HIDDEN
     x_flat = torch.empty(x_elems, dtype=torch.bfloat16, device=dev)
-    x_off = [0]
 
-    def x_view(K):
-        v = x_flat[x_off[0]:x_off[0] + T_MAIN * K].view(T_MAIN, K)
-        x_off[0] += T_MAIN * K
-        v.copy_(inputs.activations_device(gen, T_MAIN, K, dev))
-        return v
+    def x_views(flat, fill):
+        off, out = 0, []
+        for _ in range(inputs.LAYERS_9B):
+            row = []
+            for _, K, _ in inputs.LAYER_9B:
+                v = flat[off:off + T_MAIN * K].view(T_MAIN, K)
+                if fill:
+                    v.copy_(inputs.activations_device(gen, T_MAIN, K, dev))
+                row.append(v)
+                off += T_MAIN * K
+            out.append(row)
+        xh = flat[off:off + T_MAIN * HIDDEN].view(T_MAIN, HIDDEN)
+        if fill:
+            xh.copy_(inputs.activations_device(gen, T_MAIN, HIDDEN, dev))
+        return out, xh
 
-    xs = [[x_view(K) for _, K, _ in inputs.LAYER_9B] for _ in range(inputs.LAYERS_9B)]
-    x_head = x_view(HIDDEN)
+    xs, x_head = x_views(x_flat, True)
     ys = [torch.empty((T_MAIN, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_9B]
     logits_head = torch.empty((T_MAIN, VOCAB), dtype=torch.float32, device=dev)
 
@@ -319,42 +300,59 @@ def run_gpu(args):
             "tok": torch.zeros(T_MAIN + 1, dtype=torch.int32, device=dev),
         })
 
-    def gemm(w, x, y, T):
-        sv.qgemm_w4a16(ctx, w["qcodes"], w["scales"], w["zeros"], w["g"], x, y, T, w["N"], w["K"])
+    def w4_desc(w, x, y, T, wait_prev=1):
+        return {"quant": sv.SPEC_QUANT_W4, "qcodes": w["qcodes"], "scales": w["scales"],
+                "zeros": w["zeros"], "group_size": w["g"], "x": x, "y": y, "T": T, "N": w["N"],
+                "K": w["K"], "wait_prev": wait_prev}
 
-    def stack(T):
-        for l in range(inputs.LAYERS_9B):
-            for j in range(len(inputs.LAYER_9B)):
-                gemm(layers[l][j], xs[l][j][:T], ys[j][:T], T)
+    def stack_descs(T, xs_b, xh_b, with_head):
+        # every GEMM waits for its predecessor (the decoder's dependency chain)
+        d = [w4_desc(layers[l][j], xs_b[l][j][:T], ys[j][:T], T)
+             for l in range(inputs.LAYERS_9B) for j in range(len(inputs.LAYER_9B))]
+        if with_head:
+            d.append(w4_desc(head, xh_b, logits_head, T))
+        return d
+
+    st32 = sv.GemmStack(ctx, stack_descs(T_MAIN, xs, x_head, True))
+    st16 = sv.GemmStack(ctx, stack_descs(T_SMALL, xs, x_head, False))
 
     def gemm_part():
-        stack(T_MAIN)
-        gemm(head, x_head, logits_head, T_MAIN)
+        st32.run()
 
     def accept_part(i):
         a = acc_sets[i]
         sv.spec_accept(ctx, a["logits"], a["q"], a["drafts"], a["u"], T_MAIN, VOCAB, a["n"], a["tok"])
 
-    # ---- eager warm-up (also checks the device error word), then graphs
-    gemm_part()
-    for i in range(3):
-        accept_part(i)
-    stack(T_SMALL)
-    sv.spec_sync_status(ctx)
     side = torch.cuda.Stream(device=dev)
-    side.wait_stream(torch.cuda.current_stream())
-    g_gemm, g_acc, g_t16 = torch.cuda.CUDAGraph(), [torch.cuda.CUDAGraph() for _ in range(3)], \
-        torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_gemm, stream=side):
-            gemm_part()
-        for i in range(3):
-            with torch.cuda.graph(g_acc[i], stream=side):
-                accept_part(i)
-        with torch.cuda.graph(g_t16, stream=side):
-            stack(T_SMALL)
-    torch.cuda.synchronize()
-    sv.spec_sync_status(ctx)
+
+    def graph_of(fn):
+        fn()
+        sv.spec_sync_status(ctx)
+        g = torch.cuda.CUDAGraph()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(g, reps, warm=2):
+        for _ in range(warm):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        sv.spec_sync_status(ctx)
+        return e0.elapsed_time(e1) / reps
+
+    # ---- eager warm-up (also checks the device error word), then graphs
+    g_gemm = graph_of(gemm_part)
+    g_acc = [graph_of(lambda i=i: accept_part(i)) for i in range(3)]
+    g_t16 = graph_of(st16.run)
 
     K, W = args.steps, args.warmup
     for i in range(W):
@@ -382,17 +380,55 @@ def run_gpu(args):
     gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     acc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     step_ms_med = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+    sv.spec_sync_status(ctx)
+
+    # outputs of the last timed step, kept for the CPU-oracle leg's comparison
+    check_layer = inputs.LAYERS_9B - 1
+    kept = {"ys": [y.float().cpu().numpy() for y in ys], "logits": logits_head.cpu().numpy(),
+            "acc": [(int(a["n"].item()), a["tok"].cpu().numpy()) for a in acc_sets]}
 
     # ---- T=16 stack (configs' T=16 verify GEMM pass)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    K16 = max(K, 10)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(K16):
-        g_t16.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    t16_ms = e0.elapsed_time(e1) / K16
+    t16_ms = time_graph(g_t16, max(K, 10))
+
+    # ---- the same T=32 GEMMs as 145 separate calls (one launch each)
+    def per_gemm_part():
+        for l in range(inputs.LAYERS_9B):
+            for j in range(len(inputs.LAYER_9B)):
+                w = layers[l][j]
+                sv.qgemm_w4a16(ctx, w["qcodes"], w["scales"], w["zeros"], GROUP, xs[l][j], ys[j],
+                               T_MAIN, w["N"], w["K"])
+        sv.qgemm_w4a16(ctx, head["qcodes"], head["scales"], head["zeros"], GROUP, x_head, logits_head,
+                       T_MAIN, VOCAB, HIDDEN)
+
+    g_pg = graph_of(per_gemm_part)
+    pg_ms = time_graph(g_pg, max(5, min(K, 20)))
+    del g_pg
+
+    # ---- config 1 as stated: q, k, v, o, gate, up, down as seven GEMMs per
+    # layer at T=16 (q/k/v share their input, so k and v do not wait for q; up
+    # does not wait for gate).  The codes are row ranges of the fused
+    # matrices; their scales and zero points are copied into contiguous
+    # per-projection arrays.
+    def split_w(w, r0, r1):
+        return {"N": r1 - r0, "K": w["K"], "g": w["g"], "qcodes": w["qcodes"][r0:r1],
+                "scales": w["scales"][:, r0:r1].contiguous(),
+                "zeros": w["zeros"][:, r0 // 2:r1 // 2].contiguous()}
+
+    unf_descs, unf_keep = [], []
+    y_unf = [torch.empty((T_SMALL, n), dtype=torch.bfloat16, device=dev)
+             for n in (4096, 1024, 1024, 4096, 12288, 12288, 4096)]
+    for l in range(inputs.LAYERS_9B):
+        qkv, o, gu, down = layers[l]
+        parts = [(split_w(qkv, 0, 4096), 0, 1), (split_w(qkv, 4096, 5120), 0, 0),
+                 (split_w(qkv, 5120, 6144), 0, 0), (o, 1, 1), (split_w(gu, 0, 12288), 2, 1),
+                 (split_w(gu, 12288, 24576), 2, 0), (down, 3, 1)]
+        for p_i, (w, j, wp) in enumerate(parts):
+            unf_keep.append(w)
+            unf_descs.append(w4_desc(w, xs[l][j][:T_SMALL], y_unf[p_i], T_SMALL, wp))
+    st_unf = sv.GemmStack(ctx, unf_descs)
+    g_unf = graph_of(st_unf.run)
+    unf_ms = time_graph(g_unf, max(K, 10))
+    del g_unf, st_unf, unf_keep, y_unf
 
     # ---- shared-seed (Gumbel-max) acceptance of the same T=32 blocks: the
     # drafter's tokens are sampled on the GPU from log q with the same seed
@@ -410,15 +446,8 @@ def run_gpu(args):
         sv.spec_accept_gumbel(ctx, acc_sets[i]["logits"], g["drafts"], T_MAIN, VOCAB,
                               GUMBEL_SEED + i, 0, g["n"], g["tok"])
 
-    for i in range(3):
-        gumbel_part(i)
-    sv.spec_sync_status(ctx)
-    g_gum = [torch.cuda.CUDAGraph() for _ in range(3)]
-    with torch.cuda.stream(side):
-        for i in range(3):
-            with torch.cuda.graph(g_gum[i], stream=side):
-                gumbel_part(i)
-    torch.cuda.synchronize()
+    g_gum = [graph_of(lambda i=i: gumbel_part(i)) for i in range(3)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     KG = max(K, 30)
     e0.record()
     for i in range(KG):
@@ -428,10 +457,11 @@ def run_gpu(args):
     gum_ms = e0.elapsed_time(e1) / KG
     sv.spec_sync_status(ctx)
 
-    # ---- greedy tree acceptance: 4 branches x depth 8 (T=32) and 8 x 8
-    # (T=64) over V=151936, drafts matching the row argmax with p = 0.7
+    # ---- greedy tree acceptance over V=151936: T in {1, 4, 8, 16, 32, 64}
+    # nodes as max(1, T/8) branches of depth min(T, 8), drafts matching the
+    # row argmax with p = 0.7
     tree_res = []
-    for Tt in (32, 64):
+    for Tt in (1, 4, 8, 16, 32, 64):
         tin = inputs.tree_inputs(np.random.default_rng(500 + Tt), Tt, VOCAB, logit_std=3.0, p_match=0.7)
         tbuf = {"l": torch.from_numpy(tin.logits).to(dev), "d": torch.from_numpy(tin.drafts).to(dev),
                 "p": torch.from_numpy(tin.parent).to(dev),
@@ -442,30 +472,16 @@ def run_gpu(args):
         def tree_call(b=tbuf, T_=Tt):
             sv.spec_accept_tree(ctx, b["l"], b["d"], b["p"], T_, VOCAB, b["n"], b["t"], b["k"])
 
-        tree_call()
-        sv.spec_sync_status(ctx)
-        g_tree = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g_tree, stream=side):
-                tree_call()
-        torch.cuda.synchronize()
-        for _ in range(3):
-            g_tree.replay()
-        KT = max(K, 30)
-        e0.record()
-        for _ in range(KT):
-            g_tree.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        t_ms = e0.elapsed_time(e1) / KT
-        sv.spec_sync_status(ctx)
+        g_tree = graph_of(tree_call)
+        t_ms = time_graph(g_tree, max(K, 30), warm=3)
         tree_res.append({"T": Tt, "branches": max(1, Tt // 8), "depth": min(Tt, 8), "ms": round(t_ms, 5),
                          "logits_GB/s": round((Tt + 1) * VOCAB * 4 / (t_ms * 1e-3) / 1e9, 1),
                          "path_len": int(tbuf["n"].item())})
         del tbuf, g_tree
 
     # ---- 27B-class Large tier: 64 layers of per-channel int8 projections at
-    # T=32 with the block-1024 random Hadamard rotation of the activations
+    # T=32, with and without the block-1024 random Hadamard rotation of every
+    # GEMM's activations (rotated inside the same launch)
     L8 = inputs.LAYER_27B
     w8 = [[inputs.w8_weights_device(gen, N, K, dev) for _, K, N in L8] for _ in range(inputs.LAYERS_27B)]
     x8 = [inputs.activations_device(gen, T_MAIN, K, dev) for _, K, _ in L8]
@@ -473,31 +489,22 @@ def run_gpu(args):
     s8 = [torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(300 + j), K)).to(dev)
           for j, (_, K, _) in enumerate(L8)]
 
-    def stack8():
-        for l in range(inputs.LAYERS_27B):
-            for j, (_, K, N) in enumerate(L8):
-                w = w8[l][j]
-                sv.qgemm_w8a16(ctx, w["qcodes"], w["scales"], 0, x8[j], y8[j], T_MAIN, N, K, s8[j], 1024)
+    def w8_descs(rotate):
+        return [{"quant": sv.SPEC_QUANT_W8, "qcodes": w8[l][j]["qcodes"], "scales": w8[l][j]["scales"],
+                 "zeros": None, "group_size": 0, "x": x8[j], "y": y8[j], "T": T_MAIN, "N": N, "K": K,
+                 "signs": s8[j] if rotate else None, "hadamard_block": 1024 if rotate else 0,
+                 "wait_prev": 1}
+                for l in range(inputs.LAYERS_27B) for j, (_, K, N) in enumerate(L8)]
 
-    stack8()
-    sv.spec_sync_status(ctx)
-    g_w8 = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_w8, stream=side):
-            stack8()
-    torch.cuda.synchronize()
-    for _ in range(2):
-        g_w8.replay()
+    st8 = sv.GemmStack(ctx, w8_descs(True))
+    st8n = sv.GemmStack(ctx, w8_descs(False))
+    g_w8 = graph_of(st8.run)
+    g_w8n = graph_of(st8n.run)
     K8 = max(5, min(K, 20))
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(K8):
-        g_w8.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    w8_ms = e0.elapsed_time(e1) / K8
-    w8_bytes = inputs.LAYERS_27B * sum(w8_gemm_bytes(T_MAIN, N, K) + 4 * T_MAIN * K for _, K, N in L8)
-    del w8
+    w8_ms = time_graph(g_w8, K8)
+    w8n_ms = time_graph(g_w8n, K8)
+    w8_bytes = inputs.LAYERS_27B * sum(w8_gemm_bytes(T_MAIN, N, K) for _, K, N in L8)
+    del g_w8, g_w8n, st8, st8n, w8
     clocks = sampler.stop()
     sv.spec_sync_status(ctx)
 
@@ -516,26 +523,11 @@ def run_gpu(args):
         sum(v.numel() * v.element_size() for v in h_acc[0].values())
     d2h = 4 * (T_MAIN + 2)
 
-    # the second buffer set (activation views with the same layout, its own
-    # acceptance inputs) and a graph of each step part per buffer
     x_flat2 = torch.empty_like(x_flat)
-    xs2, off = [], 0
-    for _ in range(inputs.LAYERS_9B):
-        row = []
-        for _, K_, _ in inputs.LAYER_9B:
-            row.append(x_flat2[off:off + T_MAIN * K_].view(T_MAIN, K_))
-            off += T_MAIN * K_
-        xs2.append(row)
-    x_head2 = x_flat2[off:off + T_MAIN * HIDDEN].view(T_MAIN, HIDDEN)
-    xbuf = [(x_flat, xs, x_head), (x_flat2, xs2, x_head2)]
+    xs2, x_head2 = x_views(x_flat2, False)
+    x_flat2.copy_(x_flat)
+    stacks_e = [st32, sv.GemmStack(ctx, stack_descs(T_MAIN, xs2, x_head2, True))]
     ebuf = [{k: torch.empty_like(acc_sets[0][k]) for k in keys + ("n", "tok")} for _ in range(2)]
-
-    def gemm_part_on(b):
-        _, xs_b, xh_b = xbuf[b]
-        for l in range(inputs.LAYERS_9B):
-            for j in range(len(inputs.LAYER_9B)):
-                gemm(layers[l][j], xs_b[l][j], ys[j], T_MAIN)
-        gemm(head, xh_b, logits_head, T_MAIN)
 
     def accept_on(b):
         e = ebuf[b]
@@ -544,20 +536,8 @@ def run_gpu(args):
     for b in range(2):
         for k in keys:
             ebuf[b][k].copy_(acc_sets[b][k])
-    x_flat2.copy_(x_flat)
-    g_gemm_e, g_acc_e = [torch.cuda.CUDAGraph() for _ in range(2)], [torch.cuda.CUDAGraph() for _ in range(2)]
-    for b in range(2):
-        gemm_part_on(b)
-        accept_on(b)
-    sv.spec_sync_status(ctx)
-    with torch.cuda.stream(side):
-        for b in range(2):
-            with torch.cuda.graph(g_gemm_e[b], stream=side):
-                gemm_part_on(b)
-            with torch.cuda.graph(g_acc_e[b], stream=side):
-                accept_on(b)
-    torch.cuda.synchronize()
-
+    g_gemm_e = [graph_of(stacks_e[b].run) for b in range(2)]
+    g_acc_e = [graph_of(lambda b=b: accept_on(b)) for b in range(2)]
     comp = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream(device=dev)
     copied = [torch.cuda.Event() for _ in range(2)]
@@ -567,6 +547,7 @@ def run_gpu(args):
         done[b].record(comp)
     K_e2e = max(10, min(K, 200))
     e2e_evs = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    xbuf = [x_flat, x_flat2]
 
     def issue_copy(i):
         b = i % 2
@@ -574,7 +555,7 @@ def run_gpu(args):
             if i == 0:
                 copy_stream.wait_event(e2e_evs[0])
             copy_stream.wait_event(done[b])          # step i-2 has finished with buffer b
-            xbuf[b][0].copy_(h_xflat, non_blocking=True)
+            xbuf[b].copy_(h_xflat, non_blocking=True)
             for k in keys:
                 ebuf[b][k].copy_(h_acc[i % 3][k], non_blocking=True)
             copied[b].record(copy_stream)
@@ -608,7 +589,6 @@ def run_gpu(args):
     gemm_bytes = stack_bytes(T_MAIN) + head_bytes(T_MAIN)
     peak, peak_kind = hbm_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
-    launches = gemm_launches_per_step()
     accepted = []
     for a in acc_sets:
         accepted.append({"level": a["level"], "sigma": round(a["sigma"], 4),
@@ -616,11 +596,8 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        lay, xh, acc_h = host_layer0()
-        gbs, secs, desc = oracle_sample(lay, xh, acc_h, budget_s=args.cpu_budget)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": desc + f"; {secs:.1f} s; numpy BLAS threads for the matmul, the rest "
-                                f"single-threaded"}
+        cpu = cpu_oracle_leg(layers[check_layer], xs[check_layer], head, x_head, acc_sets, kept,
+                             args.cpu_budget)
 
     if rank == 0:
         out = {
@@ -644,7 +621,9 @@ def run_gpu(args):
                 "acceptance_levels": list(ACCEPT_LEVELS),
                 "l2": "inputs larger than L2 (4.08 GB of weights per step)",
                 "parallelism": f"replicas x{world}",
-                "graph": "one CUDA graph per step part (GEMM stack+head, acceptance)",
+                "graph": "one CUDA graph per step part: the GEMM stack (one persistent launch of "
+                         "all 145 GEMMs, each waiting for its predecessor) and the acceptance "
+                         "(two launches)",
             },
             "pct_of_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
             "draft_tokens_scored_per_s": round(world * T_MAIN / (ms_per_step * 1e-3), 1),
@@ -652,6 +631,13 @@ def run_gpu(args):
             "acceptance_ms": round(acc_ms, 5),
             "acceptance_share": round(acc_ms / (gemm_ms + acc_ms), 4),
             "accepted": accepted,
+            "per_gemm_launches": {
+                "workload": "the same T=32 GEMMs (36 layers + head) as 145 separate qgemm_w4a16 "
+                            "calls in one graph (no acceptance)",
+                "ms": round(pg_ms, 5),
+                "value": round(gemm_bytes / (pg_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "frac": round(gemm_bytes / (pg_ms * 1e-3) / 1e9 / peak, 4),
+            },
             "accept_gumbel": {
                 "workload": "shared-seed (Gumbel-max) acceptance of the same T=32 blocks over "
                             "V=151936: one launch reads the (T+1)xV fp32 logits once; the drafts "
@@ -668,33 +654,46 @@ def run_gpu(args):
                 "cases": tree_res,
             },
             "t16": {
-                "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance)",
+                "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance), one stack "
+                            "launch",
                 "ms_per_step": round(t16_ms, 5),
                 "value": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
                 "frac": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9 / peak, 4),
                 "draft_tokens_scored_per_s": round(T_SMALL / (t16_ms * 1e-3), 1),
             },
+            "t16_unfused": {
+                "workload": "the T=16 stack as the configuration states it: q, k, v, o, gate, up, "
+                            "down as 7 GEMMs per layer (252 GEMMs, one stack launch; k, v and up "
+                            "do not wait for the GEMM before them)",
+                "ms_per_step": round(unf_ms, 5),
+                "value": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
+                "frac": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9 / peak, 4),
+            },
             "w8_27b": {
                 "workload": "27B-class int8 per-channel stack at T=32: 64 layers (qkv 5120x7168, "
                             "o 5120x5120, gate_up 5120x34816, down 17408x5120), block-1024 random "
-                            "Hadamard rotation of every GEMM's activations (no head, no acceptance)",
+                            "Hadamard rotation of every GEMM's activations inside the launch (no "
+                            "head, no acceptance)",
                 "ms_per_step": round(w8_ms, 5),
                 "bytes_per_step": w8_bytes,
                 "value": round(w8_bytes / (w8_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
                 "frac": round(w8_bytes / (w8_ms * 1e-3) / 1e9 / peak, 4),
                 "draft_tokens_scored_per_s": round(T_MAIN / (w8_ms * 1e-3), 1),
+                "without_rotation_ms": round(w8n_ms, 5),
+                "rotation_overhead": round(w8_ms / w8n_ms - 1.0, 4),
             },
             "roofline": {
-                "kernel": "qgemm_kernel<W4, TPAD=32> (all 145 GEMM launches of a step)",
+                "kernel": "qgemm_kernel<W4, TPAD=32> (one launch: the step's 145 GEMMs)",
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                 "peak_source": f"{peak_kind} HBM copy bandwidth" +
                                (" (of fallback)" if peak_kind == "fallback" else " (of measured)"),
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": ncu_traffic("qgemm_w4_t32_verify_step"),
-                "bytes_per_launch_avg": gemm_bytes // launches,
-                "launch_ms_avg": round(gemm_ms / launches, 6),
+                "bytes_per_launch": gemm_bytes,
+                "launch_ms": round(gemm_ms, 6),
             },
             "cpu_baseline": cpu,
             "e2e": {
@@ -704,7 +703,7 @@ def run_gpu(args):
                 "staging": "double-buffered device inputs: step i+1's host-to-device copy runs on a "
                            "copy stream while step i computes; every step reads its result back",
             },
-            "gpu_launches": K * (launches + 2),
+            "gpu_launches": K * 3,
             "clocks": clocks,
         }
         print(json.dumps(out), flush=True)
@@ -712,6 +711,70 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def cpu_oracle_leg(layer, xl, head, x_head, acc_sets, kept, budget_s):
+    """The fp64 oracle on the host cores, on a bounded sample of the timed
+    step: row samples of the last layer's four GEMMs and of the LM head (the
+    same weights and activations the GPU used) and the three acceptance calls.
+    Returns the CPU baseline (throughput of the sample) together with the
+    GPU step's agreement with the oracle on that sample."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    def host_w4(w, rows):
+        # output rows in pairs (zero points pack two rows per byte)
+        pairs = rows[0::2] // 2
+        return (w["qcodes"][torch.from_numpy(rows).to(w["qcodes"].device)].cpu().numpy(),
+                w["scales"][:, torch.from_numpy(rows).to(w["scales"].device)].cpu().numpy(),
+                w["zeros"][:, torch.from_numpy(pairs).to(w["zeros"].device)].cpu().numpy())
+
+    def bits(x):
+        return x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    rng = np.random.default_rng(31)
+    gemms = [(w, x, kept["ys"][j], False) for j, (w, x) in enumerate(zip(layer, xl))]
+    gemms.append((head, x_head, kept["logits"], True))
+    t0 = time.perf_counter()
+    done_bytes, worst, checked = 0, 0.0, []
+    n_pairs = 16
+    while True:
+        for w, x, y, f32 in gemms:
+            N, K_ = w["N"], w["K"]
+            p = np.sort(rng.choice(N // 2, size=n_pairs, replace=False))
+            rows = np.stack([2 * p, 2 * p + 1], axis=1).reshape(-1)
+            qc, sc, zr = host_w4(w, rows)
+            ref = oracle.qgemm_w4a16(qc, sc, zr, GROUP, bits(x), T_MAIN, len(rows), K_)
+            got = y[:, rows]
+            allowed = 1e-2 * np.sqrt(np.mean(ref ** 2)) + (0.0 if f32 else 2.0 ** -8 * np.abs(ref))
+            worst = max(worst, float(np.max(np.abs(got - ref) / allowed)))
+            done_bytes += w4_gemm_bytes(T_MAIN, len(rows), K_, out_bytes=4 if f32 else 2)
+            checked.append(f"{N}x{K_}")
+        if time.perf_counter() - t0 > budget_s:
+            break
+        n_pairs = min(2 * n_pairs, 512)
+    acc = []
+    for a, (n_gpu, tok_gpu) in zip(acc_sets, kept["acc"]):
+        h = a["host"]
+        n_o, t_o, near = oracle.spec_accept(h.logits, h.q, h.drafts, h.u)
+        evaluated = near[:min(n_o + 1, T_MAIN)].any() or near[T_MAIN]
+        acc.append({"level": a["level"], "n_gpu": n_gpu, "n_oracle": int(n_o),
+                    "match": bool(n_gpu == n_o and list(tok_gpu[:n_gpu + 1]) == list(t_o)),
+                    "near_ties": int(near.sum()), "near_tie_decides": bool(evaluated)})
+        done_bytes += accept_bytes(T_MAIN)
+    dt = time.perf_counter() - t0
+    sample = (f"oracle (numpy fp64) on row samples of the timed step's last layer (qkv, o, gate_up, "
+              f"down) and LM head ({len(checked)} row-sampled GEMMs, up to {2 * n_pairs} rows each) "
+              f"and its three spec_accept calls over V={VOCAB}: {done_bytes / 1e6:.1f} MB of the "
+              f"step's {step_bytes() / 1e9:.2f} GB; {dt:.1f} s; numpy BLAS threads for the matmul, "
+              f"the rest single-threaded")
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": sample,
+            "parity": {"gemm_max_err_over_bar": round(worst, 4), "gemm_pass": worst <= 1.0,
+                       "accept": acc,
+                       "accept_pass": all(x["match"] or x["near_tie_decides"] for x in acc)}}
 
 
 # ----------------------------------------------------------------------------
@@ -862,6 +925,92 @@ def run_kernel_case_w8(args):
     ctx.close()
 
 
+def run_stack_case(args):
+    """One GEMM stack alone, graph-replayed warm-up + steps times: `9b32[:L]`
+    (L layers of the T=32 int4 stack plus the LM head), `9b16[:L]` (the T=16
+    stack), `27b[:L]` / `27bnr[:L]` (the int8 Large-tier stack with / without
+    rotation).  L defaults to the full depth.  Prints device time per launch
+    and bandwidth."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    name, _, depth = args.stack_case.partition(":")
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    descs, keep, nbytes = [], [], 0
+    if name in ("9b32", "9b16"):
+        T = 32 if name == "9b32" else 16
+        L = int(depth) if depth else inputs.LAYERS_9B
+        ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_9B]
+        for _ in range(L):
+            for j, (_, K, N) in enumerate(inputs.LAYER_9B):
+                w = inputs.w4_weights_device(gen, N, K, dev, GROUP)
+                x = inputs.activations_device(gen, T, K, dev)
+                keep += [w, x]
+                descs.append({"quant": sv.SPEC_QUANT_W4, "qcodes": w["qcodes"], "scales": w["scales"],
+                              "zeros": w["zeros"], "group_size": GROUP, "x": x, "y": ys[j], "T": T,
+                              "N": N, "K": K, "wait_prev": 1})
+                nbytes += w4_gemm_bytes(T, N, K)
+        if name == "9b32":
+            w = inputs.w4_weights_device(gen, VOCAB, HIDDEN, dev, GROUP)
+            x = inputs.activations_device(gen, T, HIDDEN, dev)
+            y = torch.empty((T, VOCAB), dtype=torch.float32, device=dev)
+            keep += [w, x, y]
+            descs.append({"quant": sv.SPEC_QUANT_W4, "qcodes": w["qcodes"], "scales": w["scales"],
+                          "zeros": w["zeros"], "group_size": GROUP, "x": x, "y": y, "T": T,
+                          "N": VOCAB, "K": HIDDEN, "wait_prev": 1})
+            nbytes += head_bytes(T)
+    else:
+        rot = name == "27b"
+        L = int(depth) if depth else inputs.LAYERS_27B
+        ys = [torch.empty((T_MAIN, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_27B]
+        for _ in range(L):
+            for j, (_, K, N) in enumerate(inputs.LAYER_27B):
+                w = inputs.w8_weights_device(gen, N, K, dev)
+                x = inputs.activations_device(gen, T_MAIN, K, dev)
+                s = torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(j), K)).to(dev)
+                keep += [w, x, s]
+                descs.append({"quant": sv.SPEC_QUANT_W8, "qcodes": w["qcodes"], "scales": w["scales"],
+                              "zeros": None, "group_size": 0, "x": x, "y": ys[j], "T": T_MAIN, "N": N,
+                              "K": K, "signs": s if rot else None, "hadamard_block": 1024 if rot else 0,
+                              "wait_prev": 1})
+                nbytes += w8_gemm_bytes(T_MAIN, N, K)
+    st = sv.GemmStack(ctx, descs)
+    st.run()
+    sv.spec_sync_status(ctx)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            st.run()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, _ = hbm_peak()
+    print(json.dumps({"stack_case": args.stack_case, "gemms": len(descs), "ms_per_launch": round(ms, 5),
+                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "bytes": nbytes,
+                      "prefetch": [os.environ.get("SPEC_PREFETCH_LEAD"),
+                                   os.environ.get("SPEC_PREFETCH_LEAD_FULL")]}), flush=True)
+    del g, st
+    ctx.close()
+
+
 def run_accept_case(args):
     """spec_accept alone at T drafts over V tokens, launched warm-up + steps
     times eagerly (for profiling the acceptance kernels in isolation); prints
@@ -996,6 +1145,8 @@ def main():
                     help="time spec_accept_gumbel alone at T drafts over V tokens (eager launches)")
     ap.add_argument("--kernel-case-w8", default=None, metavar="T,N,K[,B]",
                     help="time one per-channel int8 GEMM shape (B > 0: rotation block)")
+    ap.add_argument("--stack-case", default=None, metavar="NAME[:LAYERS]",
+                    help="time one GEMM stack alone: 9b32, 9b16, 27b or 27bnr, optionally fewer layers")
     ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
                     help="time one int4 GEMM shape in isolation instead of the verify step")
     args = ap.parse_args()
@@ -1010,6 +1161,9 @@ def main():
         return
     if args.kernel_case_w8:
         run_kernel_case_w8(args)
+        return
+    if args.stack_case:
+        run_stack_case(args)
         return
     if args.kernel_case:
         run_kernel_case(args)

@@ -18,18 +18,29 @@ __all__ = [
     "qgemm_w4a16", "qgemm_w8a16", "fwht_rotate", "spec_softmax", "spec_accept",
     "spec_accept_noalloc", "spec_accept_tree", "spec_gumbel_sample", "spec_accept_gumbel",
     "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
-    "SPEC_DTYPE_BF16", "SPEC_DTYPE_F32",
+    "SPEC_DTYPE_BF16", "SPEC_DTYPE_F32", "SPEC_QUANT_W4", "SPEC_QUANT_W8",
+    "GemmDesc", "GemmStack", "qgemm_stack_create", "qgemm_stack_run", "qgemm_stack_destroy",
+    "spec_set_stream_prefetch", "spec_test_stall",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
 
 SPEC_DTYPE_BF16 = 0
 SPEC_DTYPE_F32 = 1
+SPEC_QUANT_W4 = 0
+SPEC_QUANT_W8 = 1
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 _U64 = ctypes.c_uint64
+
+
+class GemmDesc(ctypes.Structure):
+    """spec_gemm_desc: one GEMM of a stack (field order as in the header)."""
+    _fields_ = [("quant", _I), ("qcodes", _P), ("scales", _P), ("zeros", _P), ("group_size", _I),
+                ("x", _P), ("y", _P), ("y_dtype", _I), ("T", _I), ("N", _I), ("K", _I),
+                ("signs", _P), ("hadamard_block", _I), ("wait_prev", _I)]
 
 # name -> argtypes (all return int status, except spec_last_error / spec_version)
 _SIGS = {
@@ -47,6 +58,11 @@ _SIGS = {
     "spec_accept_tree": [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P],
     "spec_gumbel_sample": [_P, _P, _I, _I, _U64, _U64, _P, _P, _P],
     "spec_accept_gumbel": [_P, _P, _P, _I, _I, _U64, _U64, _P, _P, _P, _P],
+    "qgemm_stack_create": [_P, ctypes.POINTER(GemmDesc), _I, ctypes.POINTER(_P)],
+    "qgemm_stack_run": [_P, _P, _P],
+    "qgemm_stack_destroy": [_P],
+    "spec_set_stream_prefetch": [_P, _I, _I],
+    "spec_test_stall": [_P, _I, _U64],
     "qdequant_w4": [_P, _P, _P, _P, _I, _I, _I, _P, _P],
     "qdequant_w8": [_P, _P, _P, _I, _I, _I, _P, _P],
 }
@@ -158,6 +174,66 @@ def qgemm_w8a16(ctx, qcodes, scales, group_size, x, y, T, N, K, signs=None, hada
     _call("qgemm_w8a16", _h(ctx), _ptr(qcodes), _ptr(scales), group_size, _ptr(x), _ptr(y),
           SPEC_DTYPE_F32 if y_f32 else SPEC_DTYPE_BF16, T, N, K, _ptr(signs), hadamard_block,
           _stream(stream))
+
+
+def _desc(d: dict) -> GemmDesc:
+    y = d["y"]
+    y_f32 = d.get("y_f32")
+    if y_f32 is None:
+        y_f32 = str(getattr(y, "dtype", "")) == "torch.float32"
+    return GemmDesc(d.get("quant", SPEC_QUANT_W4), _ptr(d["qcodes"]), _ptr(d["scales"]),
+                    _ptr(d.get("zeros")), d["group_size"], _ptr(d["x"]), _ptr(y),
+                    SPEC_DTYPE_F32 if y_f32 else SPEC_DTYPE_BF16, d["T"], d["N"], d["K"],
+                    _ptr(d.get("signs")), d.get("hadamard_block", 0), d.get("wait_prev", 1))
+
+
+class GemmStack:
+    """Owns a spec_gemm_stack: a list of GEMMs run by one launch."""
+
+    def __init__(self, ctx, descs):
+        arr = (GemmDesc * len(descs))(*[_desc(d) for d in descs])
+        h = _P()
+        _call("qgemm_stack_create", _h(ctx), arr, len(descs), ctypes.byref(h))
+        self.handle = h.value
+        self.ctx = ctx
+        self.n = len(descs)
+
+    def run(self, stream=None) -> None:
+        _call("qgemm_stack_run", _h(self.ctx), self.handle, _stream(stream))
+
+    def close(self) -> None:
+        if self.handle:
+            _call("qgemm_stack_destroy", self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def qgemm_stack_create(ctx, descs) -> GemmStack:
+    """descs: dicts with the keys of spec_gemm_desc (quant, qcodes, scales, zeros,
+    group_size, x, y, T, N, K, optional signs, hadamard_block, wait_prev (default 1),
+    y_f32 (default: from y's dtype))."""
+    return GemmStack(ctx, descs)
+
+
+def qgemm_stack_run(ctx, stack: GemmStack, stream=None) -> None:
+    _call("qgemm_stack_run", _h(ctx), stack.handle, _stream(stream))
+
+
+def qgemm_stack_destroy(stack: GemmStack) -> None:
+    stack.close()
+
+
+def spec_set_stream_prefetch(ctx, lead: int, lead_when_full: int) -> None:
+    _call("spec_set_stream_prefetch", _h(ctx), lead, lead_when_full)
+
+
+def spec_test_stall(ctx, skip_unit: int, wait_limit_ns: int) -> None:
+    _call("spec_test_stall", _h(ctx), skip_unit, wait_limit_ns)
 
 
 def fwht_rotate(ctx, x, y, T, K, signs, block, stream=None) -> None:

@@ -63,6 +63,16 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode and "-lineinfo" in cmd:
+            # the aarch64 build of nvcc 13.0 has crashed (segmentation fault)
+            # on some translation units only when line information is asked
+            # for; the code is the same without it
+            retry = [c for c in cmd if c != "-lineinfo"]
+            r2 = subprocess.run(retry, capture_output=True, text=True)
+            if r2.returncode == 0:
+                sys.stderr.write(f"note: {os.path.basename(cmd[-1])} built without -lineinfo "
+                                 f"(nvcc failed with it: {r.stderr.strip().splitlines()[-1:]})\n")
+                return retry, r2
         return cmd, r
 
     if jobs:

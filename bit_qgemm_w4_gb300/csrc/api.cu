@@ -7,11 +7,14 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "internal.hpp"
+#include "ptx.cuh"
 
 namespace sv {
 
@@ -97,9 +100,8 @@ namespace {
 
 // Workspace layout (bytes, each region 256-aligned).
 struct WsLayout {
-  size_t err, counters, partials, xrot, stats, chunks, argidx, argval, acc_counters, rowstat, rowcnt,
-      gbest, gidx, gsecond, total;
-  int slots;
+  size_t err, abort_all, exit_cnt, split_cnt, partials, done, rot_done, xprep, stats, chunks, argidx,
+      argval, acc_counters, rowstat, rowcnt, gbest, gidx, gsecond, total;
 };
 
 WsLayout layout_for(int num_sms) {
@@ -110,11 +112,14 @@ WsLayout layout_for(int num_sms) {
     off = round_up(off + bytes, 256);
     return at;
   };
-  L.slots = 4 * num_sms;   // two partial slots per CTA, two CTAs per SM
-  L.err = take(256);
-  L.counters = take(sizeof(int) * 4 * (size_t)kMaxTiles);
-  L.partials = take(sizeof(float) * (size_t)kPartialSlotFloats * L.slots);
-  L.xrot = take(sizeof(uint16_t) * (size_t)kMaxT * kMaxK);
+  L.err = take(sizeof(int));
+  L.abort_all = take(sizeof(int));
+  L.exit_cnt = take(sizeof(int));
+  L.split_cnt = take(sizeof(int) * (size_t)kSplitKeys * num_sms * kGemmWorkers);
+  L.partials = take(sizeof(float) * (size_t)kPartialSlotFloats * kSplitKeys * num_sms);
+  L.done = take(sizeof(int) * (size_t)kMaxStack);
+  L.rot_done = take(sizeof(int) * (size_t)kMaxStack);
+  L.xprep = take(sizeof(uint16_t) * (size_t)kSplitKeys * kMaxT * kMaxK);
   L.stats = take(sizeof(double) * 2 * (size_t)4096 * kAcceptChunks);
   L.chunks = take(sizeof(double) * kScanBlocks);
   L.argidx = take(sizeof(int) * (size_t)(kMaxAcceptT + 1) * kAcceptChunks);
@@ -153,8 +158,8 @@ int check_rotation(const int8_t* signs, int block, int T, int K) {
   if (block < 32 || block > 1024 || (block & (block - 1)))
     return set_error(SPEC_ERR_SHAPE, "hadamard_block %d not a power of two in [32, 1024]", block);
   if (K % block) return set_error(SPEC_ERR_SHAPE, "K=%d not a multiple of hadamard_block %d", K, block);
-  if (K > kMaxK || T > kMaxT)
-    return set_error(SPEC_ERR_SHAPE, "rotation buffer holds T<=%d, K<=%d", kMaxT, kMaxK);
+  if (K > kMaxK || 2 * T > kMaxT)
+    return set_error(SPEC_ERR_SHAPE, "rotated GEMMs take T <= %d, K <= %d", kMaxT / 2, kMaxK);
   return SPEC_OK;
 }
 
@@ -175,18 +180,25 @@ int check_gemm_common(const void* x, const void* y, int y_dtype, int T, int N, i
                        group_size, K);
   }
   if (group_size < 0) return set_error(SPEC_ERR_SHAPE, "negative group_size");
+  // int4 and grouped int8 GEMMs read their activations as fp16, prepared in
+  // the context's scratch
+  if ((w4 || group_size) && K > kMaxK)
+    return set_error(SPEC_ERR_SHAPE, "K=%d above %d for int4 or grouped int8 weights", K, kMaxK);
   return SPEC_OK;
 }
 
-int run_gemm(spec_ctx* ctx, GemmArgs& a, const int8_t* signs, int block, void* stream) {
+int run_gemm(spec_ctx* ctx, GemmArgs& a, void* stream) {
   DeviceGuard dg(ctx->device);
   if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (signs) {
-    SV_TRY(launch_fwht(ctx, a.x, ctx->xrot, a.T, a.K, signs, block, s));
-    a.x = ctx->xrot;
-  }
-  return launch_qgemm(ctx, a, s);
+  return launch_qgemm(ctx, a, static_cast<cudaStream_t>(stream));
+}
+
+// Reads a positive integer tuning knob from the environment (0 if unset).
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return 0;
+  const long x = std::strtol(v, nullptr, 10);
+  return x > 0 && x < 1 << 20 ? (int)x : 0;
 }
 
 }  // namespace
@@ -231,10 +243,15 @@ int spec_create(int device, size_t workspace_bytes, spec_ctx** out) {
     return set_error(SPEC_ERR_CUDA, "workspace initialisation failed");
   }
   ctx->err = reinterpret_cast<int*>(ctx->ws + L.err);
-  ctx->tile_counters = reinterpret_cast<int*>(ctx->ws + L.counters);
+  ctx->abort_all = reinterpret_cast<int*>(ctx->ws + L.abort_all);
+  ctx->exit_cnt = reinterpret_cast<int*>(ctx->ws + L.exit_cnt);
+  ctx->split_cnt = reinterpret_cast<int*>(ctx->ws + L.split_cnt);
   ctx->partials = reinterpret_cast<float*>(ctx->ws + L.partials);
-  ctx->max_slots = L.slots;
-  ctx->xrot = reinterpret_cast<uint16_t*>(ctx->ws + L.xrot);
+  ctx->done = reinterpret_cast<int*>(ctx->ws + L.done);
+  ctx->rot_done = reinterpret_cast<int*>(ctx->ws + L.rot_done);
+  if (const int v = env_int("SPEC_PREFETCH_LEAD")) ctx->pf_dist = v;
+  if (const int v = env_int("SPEC_PREFETCH_LEAD_FULL")) ctx->pf_max = v;
+  ctx->xprep = reinterpret_cast<uint16_t*>(ctx->ws + L.xprep);
   ctx->acc_stats = reinterpret_cast<double*>(ctx->ws + L.stats);
   ctx->acc_chunks = reinterpret_cast<double*>(ctx->ws + L.chunks);
   ctx->acc_argmax = reinterpret_cast<int*>(ctx->ws + L.argidx);
@@ -270,9 +287,8 @@ int spec_sync_status(spec_ctx* ctx, void* stream) {
   int err = 0;
   SV_TRY(check_cuda(cudaMemcpy(&err, ctx->err, sizeof(int), cudaMemcpyDeviceToHost), "read error word"));
   if (err == 0) return SPEC_OK;
-  cudaMemset(ctx->err, 0, sizeof(int));
-  cudaMemset(ctx->tile_counters, 0, sizeof(int) * 4 * (size_t)kMaxTiles);
-  cudaMemset(ctx->partials, 0, sizeof(float) * (size_t)kPartialSlotFloats * ctx->max_slots);
+  const WsLayout L = layout_for(ctx->num_sms);
+  cudaMemset(ctx->ws, 0, L.xprep);   // error word, abort flag, split-tile sums and every counter
   cudaMemset(ctx->acc_counters, 0, sizeof(int) * 16);
   cudaMemset(ctx->acc_rowcnt, 0, sizeof(int) * 4096);
   cudaDeviceSynchronize();
@@ -291,8 +307,9 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales, co
   SV_TRY(check_ptr(zeros, 16, "zeros"));
   SV_TRY(check_gemm_common(x, y, y_dtype, T, N, K, group_size, true));
   SV_TRY(check_rotation(signs, hadamard_block, T, K));
-  GemmArgs a{kW4, qcodes, scales, zeros, group_size, x, y, y_dtype == SPEC_DTYPE_F32, T, N, K};
-  return run_gemm(ctx, a, signs, hadamard_block, stream);
+  GemmArgs a{kW4, qcodes, scales, zeros, group_size, x, y, y_dtype == SPEC_DTYPE_F32, T, N, K,
+             signs, hadamard_block, 0};
+  return run_gemm(ctx, a, stream);
 }
 
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales, int group_size,
@@ -304,8 +321,123 @@ int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales, int
   SV_TRY(check_ptr(scales, 16, "scales"));
   SV_TRY(check_gemm_common(x, y, y_dtype, T, N, K, group_size, false));
   SV_TRY(check_rotation(signs, hadamard_block, T, K));
-  GemmArgs a{kW8, qcodes, scales, nullptr, group_size, x, y, y_dtype == SPEC_DTYPE_F32, T, N, K};
-  return run_gemm(ctx, a, signs, hadamard_block, stream);
+  GemmArgs a{kW8, qcodes, scales, nullptr, group_size, x, y, y_dtype == SPEC_DTYPE_F32, T, N, K,
+             signs, hadamard_block, 0};
+  return run_gemm(ctx, a, stream);
+}
+
+int qgemm_stack_create(spec_ctx* ctx, const spec_gemm_desc* descs, int n, spec_gemm_stack** out) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (!out) return set_error(SPEC_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (!descs) return set_error(SPEC_ERR_ARG, "descs is null");
+  if (n < 1 || n > kMaxStack) return set_error(SPEC_ERR_SHAPE, "n=%d outside 1..%d", n, kMaxStack);
+  const int quant = descs[0].quant;
+  if (quant != SPEC_QUANT_W4 && quant != SPEC_QUANT_W8)
+    return set_error(SPEC_ERR_ARG, "descs[0].quant %d is not SPEC_QUANT_W4/W8", quant);
+  int tpad = 16, run = 0;
+  for (int i = 0; i < n; ++i) {
+    const spec_gemm_desc& d = descs[i];
+    const bool w4 = d.quant == SPEC_QUANT_W4;
+    if (d.quant != quant) return set_error(SPEC_ERR_ARG, "descs[%d]: every GEMM of a stack has one quant", i);
+    SV_TRY(check_ptr(d.qcodes, 16, "qcodes"));
+    SV_TRY(check_ptr(d.scales, 16, "scales"));
+    if (w4) SV_TRY(check_ptr(d.zeros, 16, "zeros"));
+    SV_TRY(check_gemm_common(d.x, d.y, d.y_dtype, d.T, d.N, d.K, d.group_size, w4));
+    SV_TRY(check_rotation(d.signs, d.hadamard_block, d.T, d.K));
+    GemmArgs probe{};
+    probe.quant = quant == SPEC_QUANT_W4 ? kW4 : kW8;
+    probe.group_size = d.group_size;
+    probe.T = d.T;
+    probe.signs = d.signs;
+    const int tp = gemm_tpad(probe);
+    if (tp > tpad) tpad = tp;
+    // split-tile slots are keyed by entry index mod kSplitKeys: at most that
+    // many entries may be in flight at once
+    run = (i > 0 && !d.wait_prev) ? run + 1 : 0;
+    if (run >= kSplitKeys)
+      return set_error(SPEC_ERR_ARG, "descs[%d]: more than %d consecutive entries without wait_prev", i,
+                       kSplitKeys - 1);
+  }
+  DeviceGuard dg(ctx->device);
+  if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
+  std::vector<GemmEntry> host(n);
+  spec_gemm_stack* st = new (std::nothrow) spec_gemm_stack();
+  if (!st) return set_error(SPEC_ERR_OOM, "host allocation failed");
+  st->ctx = ctx;
+  st->quant = quant == SPEC_QUANT_W4 ? kW4 : kW8;
+  st->tpad = tpad;
+  st->n = n;
+  for (int i = 0; i < n; ++i) {
+    const spec_gemm_desc& d = descs[i];
+    GemmArgs a{st->quant, d.qcodes, d.scales, d.zeros, d.group_size, d.x, d.y,
+               d.y_dtype == SPEC_DTYPE_F32, d.T, d.N, d.K, d.signs, d.hadamard_block, d.wait_prev};
+    const int rc = build_entry(ctx, a, tpad, i % kSplitKeys, &host[i]);
+    if (rc) {
+      delete st;
+      return rc;
+    }
+    if (host[i].prep) st->any_prep = 1;
+  }
+  if (cudaMalloc(&st->dev_entries, sizeof(GemmEntry) * (size_t)n) != cudaSuccess) {
+    delete st;
+    return set_error(SPEC_ERR_OOM, "cudaMalloc of the stack's %d entries failed", n);
+  }
+  if (cudaMemcpy(st->dev_entries, host.data(), sizeof(GemmEntry) * (size_t)n, cudaMemcpyHostToDevice) !=
+      cudaSuccess) {
+    cudaFree(st->dev_entries);
+    delete st;
+    return set_error(SPEC_ERR_CUDA, "copy of the stack's entries failed");
+  }
+  *out = st;
+  return SPEC_OK;
+}
+
+int qgemm_stack_run(spec_ctx* ctx, const spec_gemm_stack* stack, void* stream) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (!stack) return set_error(SPEC_ERR_ARG, "stack is null");
+  if (stack->ctx != ctx) return set_error(SPEC_ERR_ARG, "stack was created on another context");
+  DeviceGuard dg(ctx->device);
+  if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
+  return launch_qgemm_stack(ctx, stack, static_cast<cudaStream_t>(stream));
+}
+
+int qgemm_stack_destroy(spec_gemm_stack* stack) {
+  clear_error();
+  if (!stack) return SPEC_OK;
+  int rc = SPEC_OK;
+  {
+    DeviceGuard dg(stack->ctx->device);
+    if (stack->dev_entries && cudaFree(stack->dev_entries) != cudaSuccess)
+      rc = set_error(SPEC_ERR_CUDA, "cudaFree failed");
+  }
+  delete stack;
+  return rc;
+}
+
+int spec_set_stream_prefetch(spec_ctx* ctx, int lead, int lead_when_full) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (lead < 0 || lead_when_full < lead || lead_when_full > 256)
+    return set_error(SPEC_ERR_ARG, "prefetch leads %d/%d outside 0 <= lead <= lead_when_full <= 256",
+                     lead, lead_when_full);
+  ctx->pf_dist = lead;
+  ctx->pf_max = lead_when_full;
+  return SPEC_OK;
+}
+
+int spec_test_stall(spec_ctx* ctx, int skip_unit, uint64_t wait_limit_ns) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (skip_unit < -1) return set_error(SPEC_ERR_ARG, "skip_unit %d < -1", skip_unit);
+  if (wait_limit_ns < 100000ull || wait_limit_ns > kWaitLimitNs)
+    return set_error(SPEC_ERR_ARG, "wait limit %llu ns outside [1e5, %llu]",
+                     (unsigned long long)wait_limit_ns, (unsigned long long)kWaitLimitNs);
+  ctx->test_skip_unit = skip_unit;
+  ctx->test_wait_ns = wait_limit_ns;
+  return SPEC_OK;
 }
 
 int fwht_rotate(spec_ctx* ctx, const uint16_t* x, uint16_t* y, int T, int K, const int8_t* signs,

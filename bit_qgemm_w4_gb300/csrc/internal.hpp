@@ -14,10 +14,12 @@ namespace sv {
 
 constexpr int kMaxT = 64;                    // largest draft block of the GEMMs
 constexpr int kTileM = 128;                  // weight rows per MMA tile
-constexpr int kStageK = 64;                  // k per pipeline stage
+constexpr int kGroupK = 64;                  // k per MMA group (one fp32 partial)
 constexpr int kPartialSlotFloats = kMaxT * kTileM;
 constexpr int kMaxK = 32768;                 // rotated-activation buffer width
-constexpr int kMaxTiles = (1 << 22) / kTileM;
+constexpr int kSplitKeys = 4;                // GEMMs of one launch whose split tiles may overlap
+constexpr int kGemmWorkers = 8;              // dequant/epilogue warps per CTA
+constexpr int kMaxStack = 1024;              // GEMMs per stack launch
 constexpr int kMaxAcceptT = 256;
 constexpr int kAcceptChunks = 64;            // max V-chunks per row in the acceptance kernels
 constexpr int kScanBlocks = 256;             // max blocks of the residual scan
@@ -41,11 +43,55 @@ struct GemmArgs {
   const uint16_t* scales;
   const uint8_t* zeros;   // W4 only
   int group_size;         // 0 = per output channel (W8 only)
-  const uint16_t* x;      // bf16 [T][K] (already rotated if requested)
+  const uint16_t* x;      // bf16 [T][K]
   void* y;
   int y_f32;
   int T, N, K;
+  const int8_t* signs;    // rotation signs [K] or null
+  int rot_block;          // Hadamard block (0 = no rotation)
+  int wait_prev;          // stack entries: read x only after the earlier GEMMs completed
 };
+
+// One GEMM as the verify kernel sees it: tensor maps and derived sizes.  A
+// single call passes one entry as a kernel parameter; a stack keeps an array
+// of them in device memory.
+struct alignas(64) GemmEntry {
+  CUtensorMap tm_x;        // activations (or their rotated copy) [T][K] bf16, box [TPAD][64]
+  CUtensorMap tm_codes;    // codes [N][K/2] (int4) or [N][K] (int8), box [128][128 bytes]
+  CUtensorMap tm_scales;   // scales [K/g][N] fp16, box [rows][128]
+  CUtensorMap tm_zeros;    // int4 zero points [K/g][N/2], box [rows][64]
+  const uint16_t* x;       // activations as given
+  const int8_t* signs;     // rotation signs, null = no rotation
+  uint16_t* xprep;         // the activations in the MMA's operand form (rotated and/or
+                           // converted to fp16), which tm_x then points at; null = x as given
+  const uint16_t* chscale; // per-output-channel int8 scales [N] (group_size 0), else null
+  void* y;
+  int T, N, K;
+  int rot_block;           // Hadamard block, 0 = none
+  float rot_scale;         // 1/sqrt(rot_block)
+  int ks;                  // stages per 128-row tile
+  int tiles;
+  int units;               // tiles * ks
+  int gshift;              // log2(group_size): group row of a stage's first k
+  int gsh;                 // row of 64-k group j inside a stage's scale box = (64 j) >> gsh
+  int scale_rows;          // rows of a stage's scale box (0 = per-channel scales)
+  uint32_t tx_w;           // TMA bytes of one stage's codes, scales and zero points
+  int y_f32;
+  int wait_prev;
+  int kind;                // operand form: kGemmBf16, kGemmF16Nib or kGemmF16
+  int prep;                // activations prepared inside the launch: 0 none, 1 rotated, 2 converted
+  uint32_t idesc;          // tcgen05.mma instruction descriptor (operand types, M, N)
+};
+
+// Operand forms of the verify GEMM's MMAs:
+//  kGemmBf16   exact int8 codes and the bf16 activations as given (int8 with
+//              one scale per output channel, applied to the fp32 sums)
+//  kGemmF16Nib int4: weights (code - zero) * scale rounded once to fp16;
+//              activations in fp16, the columns k % 8 in {2, 3, 6, 7} divided
+//              by 16 (their weights are read with a factor 16)
+//  kGemmF16    int8 with group scales: code * scale rounded to fp16, fp16
+//              activations
+enum GemmKind { kGemmBf16 = 0, kGemmF16Nib = 1, kGemmF16 = 2 };
 
 }  // namespace sv
 
@@ -55,10 +101,18 @@ struct spec_ctx {
   size_t ws_bytes = 0;
   uint8_t* ws = nullptr;
   int* err = nullptr;             // device error word
-  int* tile_counters = nullptr;   // [kMaxTiles][4] split-K arrival counters (per lane quadrant)
-  float* partials = nullptr;      // [max_slots][kPartialSlotFloats]
-  int max_slots = 0;
-  uint16_t* xrot = nullptr;       // [kMaxT][kMaxK] rotated activations
+  float* partials = nullptr;      // [kSplitKeys][num_sms][kPartialSlotFloats] split-tile sums
+  int* split_cnt = nullptr;       // [kSplitKeys][num_sms][kGemmWorkers] split-tile arrivals
+  int* done = nullptr;            // [kMaxStack] finished tile parts per stack entry
+  int* rot_done = nullptr;        // [kMaxStack] CTAs that rotated their share per entry
+  int* exit_cnt = nullptr;        // CTAs that left the last launch (resets the two above)
+  int* abort_all = nullptr;       // raised by a CTA whose wait ran out
+  int pf_dist = 4;                // GEMM weight stream: L2 prefetch lead (stages)
+  int pf_max = 16;                // ... and the lead allowed while the shared-memory ring is full
+  unsigned long long test_wait_ns = 0;   // test hook: wait limit of the next GEMM launch
+  int test_skip_unit = -1;               // test hook: unit whose weights CTA 0 never loads
+  uint16_t* xprep = nullptr;      // [kSplitKeys][kMaxT][kMaxK] prepared activations, keyed
+                                  // like the split-tile slots by a GEMM's index in its launch
   double* acc_stats = nullptr;    // [rows][kAcceptChunks][2] (max, sum) partials
   double* acc_chunks = nullptr;   // [kScanBlocks] residual chunk sums
   int* acc_argmax = nullptr;      // [kMaxAcceptT+1][kAcceptChunks] argmax partial index
@@ -71,8 +125,20 @@ struct spec_ctx {
   float* gum_second = nullptr;
 };
 
+struct spec_gemm_stack {
+  spec_ctx* ctx = nullptr;
+  int quant = 0;
+  int tpad = 0;
+  int n = 0;
+  int any_prep = 0;
+  sv::GemmEntry* dev_entries = nullptr;   // [n] in device memory
+};
+
 namespace sv {
+int build_entry(spec_ctx* ctx, const GemmArgs& a, int tpad, int index, GemmEntry* out);
+int gemm_tpad(const GemmArgs& a);   // MMA N of a GEMM: T (2T when rotated) rounded up to 16
 int launch_qgemm(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s);
+int launch_qgemm_stack(spec_ctx* ctx, const spec_gemm_stack* st, cudaStream_t s);
 int launch_fwht(spec_ctx* ctx, const uint16_t* x, uint16_t* y, int T, int K, const int8_t* signs,
                 int block, cudaStream_t s);
 int launch_softmax(spec_ctx* ctx, const float* logits, float* probs, int rows, int V,

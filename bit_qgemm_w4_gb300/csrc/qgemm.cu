@@ -3,48 +3,59 @@
 //
 // What it computes ("Karpathy's Trick for Faster Local LLMs Finally Has Proper
 // Tooling", section "How Uzu optimizes bytes and tokens per pass": 4-bit
-// asymmetric Medium tier, 8-bit symmetric Large tier, one scale per group):
-//   y[t][n] = sum_k x[t][k] * (code[n][k] - zero[g][n]) * scale[g][n]   (int4)
-//   y[t][n] = sum_k x[t][k] *  code[n][k]              * scale         (int8)
+// asymmetric Medium tier, 8-bit symmetric Large tier, one scale per group,
+// optional random Hadamard rotation of the activations):
+//   y[t][n] = sum_k x'[t][k] * (code[n][k] - zero[g][n]) * scale[g][n]   (int4)
+//   y[t][n] = sum_k x'[t][k] *  code[n][k]              * scale         (int8)
+// x' = x, or its block rotation (1/sqrt(B)) H_B (s .* x) per block of B k.
 //
-// Design (swap-AB: 128 weight rows are the MMA's M dimension, the T drafted
-// positions its N dimension; one CTA per SM owns all 512 TMEM columns):
-//  * two TMA warps stream stages into a shared-memory ring: one issues per
-//    stage the 128-byte line of codes of each of the 128 weight rows (256 k
-//    of int4 or 128 k of int8 -- full-width HBM bursts) and the stage's scale
-//    and zero rows, the other the stage's bf16 activation boxes, each on its
-//    own barrier (one issuing thread that also issued the activation boxes
-//    kept too few weight bytes in flight to stream at full HBM rate);
-//  * eight dequantisation warps (two per TMEM lane quadrant, one weight row
-//    per thread) turn codes into exact bf16 integers (code - zero, or the
-//    int8 code) and write them straight into a TMEM ring with tcgen05.st --
-//    the MMA's A operand lives in TMEM, so dequantised weights never touch
-//    shared memory, and the activations are used as stored;
-//  * one MMA warp per 64-k group issues that group's four K16 MMAs into the
-//    group's own fp32 partial (a ring of per-stage partial sets in TMEM);
-//  * four epilogue warps read each stage's partials back (tcgen05.ld) and add
-//    scale * partial into fp32 registers, so group scales are applied
-//    exactly in fp32: apart from the order of fp32 additions the result is
-//    the exact product sum (rounding the weights to bf16 instead would put
-//    the largest output error near the 1e-2 * RMS parity bound);
-//  * work is split stream-K style: the (tile, stage) units of the GEMM are
-//    divided evenly over the persistent grid; a tile cut between CTAs is
-//    summed with red.global.add into an fp32 slot and finished by the last
-//    contributor to arrive (no CTA ever waits for another);
-//  * launches overlap: the kernel is launched with programmatic stream
-//    serialisation, lets the next kernel be scheduled at once, and waits for
-//    the previous kernel only before it reads activations or writes outputs
-//    and split-tile sums -- the weight stream (which no kernel writes) never
-//    waits, so a CTA that starts on an SM freed by the previous GEMM fills
-//    its ring with weights while that GEMM's last CTAs finish.
-// Every wait is bounded (see ptx.cuh); a timeout records an error, drains the
-// CTA's in-flight copies/MMAs and frees its tensor memory before returning.
+// One persistent launch runs one GEMM or a whole stack of them (a verify
+// pass: every projection of every layer, in order).  The pass "streams every
+// weight ... once" ("Why batch-one decoding is memory-bound"), so the design
+// keeps the weight stream running across GEMM boundaries:
+//  * every GEMM's (128-row tile, k-stage) units are divided evenly over the
+//    grid (one CTA per SM); each CTA walks its share of GEMM 0, then of GEMM
+//    1, and so on;
+//  * a weight-producer warp issues, per stage, one TMA copy of the 128 rows'
+//    128-byte code lines plus the stage's scale and zero rows into a ring of
+//    shared-memory slots, and keeps the stream further ahead with L2
+//    prefetches of the boxes it will load next;
+//  * an activation-producer warp loads each stage's activation boxes
+//    (128-byte swizzle, the MMA's B operand) into a second ring; before the
+//    first load of a GEMM that depends on its predecessors it waits until
+//    those have written every output tile (device-side counters); when the
+//    MMA reads the activations in another form (fp16 for int4, or rotated)
+//    every CTA first writes its share of that form into a scratch copy (the
+//    rotation with the warp-shuffle fast Walsh-Hadamard transform) and the
+//    loads read the copy once all shares are in;
+//  * eight worker warps (two per TMEM lane quadrant, one weight row per
+//    thread) dequantise each stage straight into a TMEM ring that is the
+//    MMA's A operand: for int4 the group scale is folded in, (code - zero) *
+//    scale rounded once to fp16 (11 significant bits), so one fp32
+//    accumulator serves a whole tile and nothing is read back per stage;
+//    int8 codes with one scale per output channel enter exactly (bf16) and
+//    the scale multiplies the fp32 sums;
+//  * MMA warps (one per 64-k group for int4) issue the K16 MMAs
+//    (tcgen05.mma kind::f16, M = 128 weight rows, N = T padded to 16), all
+//    adding into one fp32 accumulator of the tile (the tensor pipe applies
+//    the MMAs one at a time, so their order does not matter); the
+//    accumulator is double buffered between a CTA's tile segments, and the
+//    workers zero it after reading it;
+//  * at the end of a segment the workers write a whole tile directly, or add
+//    a tile shared with other CTAs into an fp32 slot with red.global.add,
+//    the last contributor to arrive finishing it.
+// Every wait is bounded; a timeout records an error, raises a grid-wide
+// abort flag, drains the CTA's in-flight copies and MMAs and frees its
+// tensor memory before returning.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <cmath>
+#include <cstring>
 
+#include "fwht.cuh"
 #include "internal.hpp"
 #include "ptx.cuh"
 
@@ -56,75 +67,174 @@ constexpr int kTmemCols = 512;
 template <int QUANT, int TPAD>
 struct Cfg {
   static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k groups per stage
-  static constexpr int kStageKK = 64 * kSub;                    // k per stage
-  static constexpr int kCodeBytes = kTileM * 128;               // 128 code bytes per row
-  static constexpr int kXBoxBytes = TPAD * 128;                 // TPAD rows x 64 activations
-  static constexpr int kXOff = 0;
-  static constexpr int kCodeOff = kSub * kXBoxBytes;
-  static constexpr int kScaleOff = kCodeOff + kCodeBytes;       // [SR][128] fp16
-  static constexpr int kMaxSR = kSub;                           // scale rows per stage (g = 64)
-  static constexpr int kZeroOff = kScaleOff + kMaxSR * kTileM * 2;   // [SR][64] bytes
-  static constexpr int kStageBytes =
-      (kZeroOff + (QUANT == kW4 ? kMaxSR * 64 : 0) + 1023) / 1024 * 1024;
-  static constexpr int kCtrlBytes = 1024;
-  static constexpr int kSmemBudget = 224 * 1024;
-  static constexpr int kStagesFit = (kSmemBudget - kCtrlBytes - 1024) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
-  // warps: weight producer, dequant, MMA issue (one per 64-k group),
-  // epilogue, activation producer
-  static constexpr int kDqWarps = 8;                            // two per TMEM lane quadrant
-  static constexpr int kGroupsPerDq = kSub / 2;                 // 64-k groups of a stage per dequant warp
-  static constexpr int kMmaWarps = kSub;
-  static constexpr int kDqWarp0 = 1;
-  static constexpr int kMmaWarp0 = kDqWarp0 + kDqWarps;
-  static constexpr int kEpWarp0 = kMmaWarp0 + kMmaWarps;
-  static constexpr int kXWarp = kEpWarp0 + 4;
-  static constexpr int kThreads = 32 * (kXWarp + 1);
-  // TMEM: a ring of A slots (one stage each, 32 columns per group) and a ring
-  // of partial sets (one stage each, TPAD columns per group).
+  static constexpr int kStageKK = kGroupK * kSub;               // k per stage (128 code bytes per row)
+  static constexpr int kWorkersPerQ = kGemmWorkers / 4;         // workers per TMEM lane quadrant
+  static constexpr int kGpw = kSub / kWorkersPerQ;              // 64-k groups a worker dequantises
+  static constexpr int kCols = TPAD / kWorkersPerQ;             // accumulator columns a worker reads
+  // MMA warps: one per group for int4 up to T = 32 (a thread issues one
+  // tcgen05.mma every ~50-75 cycles), else two; each owns an accumulator
+  static constexpr int kMmaW = (QUANT == kW4 && TPAD <= 32) ? 4 : 2;
+  static constexpr int kGpm = kSub / kMmaW;                     // groups per MMA warp
+  // weight slot: codes [128 rows][128 B] (128-byte swizzle) | scales [<=kSub][128] fp16 | zeros [<=kSub][64]
+  static constexpr int kScaleOff = kTileM * 128;
+  static constexpr int kZeroOff = kScaleOff + kSub * kTileM * 2;
+  static constexpr int kWSlot = (kZeroOff + (QUANT == kW4 ? kSub * 64 : 0) + 1023) / 1024 * 1024;
+  // activation slot: kSub boxes [TPAD][64] 16-bit (128-byte rows, 128-byte swizzle)
+  static constexpr int kXBox = TPAD * 128;
+  static constexpr int kXSlot = kSub * kXBox;
+  static constexpr int kXSlots = kXSlot > 16384 ? 2 : 4;
+  static constexpr int kCtrl = 1024;
+  static constexpr int kSmemBudget = 225 * 1024;
+  static constexpr int kWSlotsFit = (kSmemBudget - 1024 - kCtrl - kXSlots * kXSlot) / kWSlot;
+  static constexpr int kWSlots = kWSlotsFit > 12 ? 12 : kWSlotsFit;
+  static constexpr int kSmemBytes = 1024 + kXSlots * kXSlot + kWSlots * kWSlot + kCtrl;
+  // TMEM: two accumulators of TPAD columns (a CTA's consecutive tile
+  // segments alternate between them; every MMA warp adds into the current
+  // one), then from column 128 a ring of A slots (one stage each, 32 columns
+  // per group)
+  static constexpr int kDCols = TPAD;
   static constexpr int kACols = 32 * kSub;
-  static constexpr int kDCols = TPAD * kSub;
-  static constexpr int kNumDFit = (kTmemCols - 2 * kACols) / kDCols;
-  static constexpr int kNumD = kNumDFit > 4 ? 4 : kNumDFit;
-  static constexpr int kNumAFit = (kTmemCols - kNumD * kDCols) / kACols;
-  static constexpr int kNumA = kNumAFit > 4 ? 4 : kNumAFit;
-  static constexpr int kD0 = kNumA * kACols;
-  // When the A ring is no deeper than the partial ring, the completion of
-  // stage n's MMAs (the partial ring's "full" barrier) also frees stage n's A
-  // slot, so the MMA warps commit one barrier per stage instead of two.
-  static constexpr bool kAFromD = kNumA <= kNumD;
-  static_assert(kStages >= 3, "pipeline too shallow");
-  static_assert(kNumA >= 2 && kNumD >= 1, "TMEM rings too shallow");
-  static_assert(kD0 + kNumD * kDCols <= kTmemCols, "TMEM budget");
+  static constexpr int kA0 = 128;
+  static constexpr int kNAFit = (kTmemCols - kA0) / kACols;
+  static constexpr int kNA = kNAFit > 4 ? 4 : kNAFit;
+  // warps: weight producer, activation producer, the TMEM owner, an idle
+  // warp (it keeps the MMA and worker warps on four-warp boundaries), the MMA
+  // warps, then the workers (any eight consecutive warps cover each TMEM lane
+  // quadrant twice)
+  static constexpr int kWProd = 0, kXProd = 1, kAlloc = 2, kMma0 = 4;
+  static constexpr int kWorker0 = kMma0 + kMmaW;
+  static constexpr int kThreads = 32 * (kWorker0 + kGemmWorkers);
+  // one CTA per SM: the register file split evenly over its threads (a
+  // launch reserves registers for whole groups of four warps)
+  static constexpr int kRegThreads = (kThreads + 127) / 128 * 128;
+  static constexpr int kMaxRegs = (65536 / kRegThreads) / 8 * 8 > 232 ? 232 : (65536 / kRegThreads) / 8 * 8;
+  static_assert(kXBox % 1024 == 0, "activation boxes must keep the 1024-byte swizzle period");
+  static_assert(kWSlots >= 4, "weight ring too shallow");
+  static_assert(kNA >= 2 && 2 * kDCols <= kA0 && kA0 + kNA * kACols <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert((3 * kStages + 2 * kNumA + 2 * kNumD) * 8 + 8 <= kCtrlBytes, "barrier block");
+  static_assert(kCols % 8 == 0, "epilogue columns in multiples of 8");
+  static constexpr int kDM = 4;                                 // ring of per-stage "MMAs done" barriers
+  static_assert(kNA <= kDM && kXSlots <= kDM, "a slot is reused within the done ring");
+  static_assert((2 * kWSlots + kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
 };
 
 struct Params {
-  int T, N, K;
-  int group_size;      // 0 = per output channel
-  int gshift;          // log2(group_size) (group_size is a power of two)
-  int ks;              // stages per tile = ceil(K / stage k)
-  int last_nsub;       // valid 64-k groups in a tile's last stage
-  int gsh;             // row of group j in a stage's scale/zero box = (64 j) >> gsh
-  int total;           // tiles * ks units (< 2^28)
-  uint32_t tx_w;       // TMA bytes of a stage's codes, scales and zero points
-  const uint16_t* scales;   // per-channel int8 scales (applied at the end of a segment)
-  void* y;
-  int y_f32;
-  float* partials;     // split tiles: [first contributor CTA][TPAD][128] fp32, kept zeroed
-  int* counters;       // per tile arrival counters, kept zeroed
+  const GemmEntry* entries;   // stack: device array; null: the entry passed by value
+  int n_entries;
+  int gate;                   // stack launch: count finished tiles, honour wait_prev
+  int any_prep;               // some entry prepares its activations (rotation counters in use)
+  int slot_ctas;              // CTAs per key in the split-tile slot arrays
+  float* partials;            // [kSplitKeys][slot_ctas][128][TPAD] fp32, kept zeroed
+  int* split_cnt;             // [kSplitKeys][slot_ctas][kGemmWorkers], kept zeroed
+  int* done;                  // [n_entries] finished (tile, worker) parts
+  int* rot_done;              // [n_entries] CTAs whose rotation share is written
+  int* exit_cnt;
   int* err;
+  int* abort_all;
+  unsigned long long wait_ns;
+  int skip_unit;              // test hook: CTA 0 never loads the weights of this unit (-1: none)
+  int pf_dist;                // L2 prefetch lead (units) while the ring has room
+  int pf_max;                 // lead allowed while the ring is full
 };
 
+// Abort state shared by a CTA's waits.
+struct Ctl {
+  volatile int* abort_cta;
+  int* abort_all;
+  int* err;
+  unsigned long long limit;
+  __device__ __forceinline__ bool aborted() const {
+    if (*abort_cta) return true;
+    if (*reinterpret_cast<volatile int*>(abort_all)) {
+      *abort_cta = 1;
+      return true;
+    }
+    return false;
+  }
+  __device__ __forceinline__ void raise() const {
+    *abort_cta = 1;
+    atomicCAS(err, 0, kDevErrTimeout);
+    atomicExch(abort_all, 1);
+  }
+};
+
+// Wait for a barrier phase; false on abort or when the limit passes.  A
+// phase that is not complete at the first probe is probed again after a
+// sleep that doubles up to `max_sleep_ns` (a probe returns at once here, and
+// a warp probing in a tight loop takes issue slots from the warps doing the
+// work); the abort flags and the clock are looked at on every eighth probe.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c,
+                                         uint32_t max_sleep_ns = 128) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  uint32_t ns = 16;
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(ns);
+    if (ns < max_sleep_ns) ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 7u) == 0) {
+      if (c.aborted()) return false;
+      if (globaltimer() - t0 > c.limit) {
+        c.raise();
+        return false;
+      }
+    }
+  }
+}
+
+// The same for a whole warp: every lane waits, and the outcome is uniform.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Ctl& c,
+                                          uint32_t max_sleep_ns = 128) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, c, max_sleep_ns));
+}
+
+// Wait until a device counter reaches `target` (acquire); false on abort or
+// when the limit passes.
+__device__ __forceinline__ bool wait_count(const int* p, int target, const Ctl& c) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  unsigned ns = 16;
+  while (true) {
+    __nanosleep(ns);
+    if (ns < 128) ns <<= 1;
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (c.aborted()) return false;
+    if (globaltimer() - t0 > c.limit) {
+      c.raise();
+      return false;
+    }
+  }
+}
+
+// Drain wait: ignores the abort flags, gives up after kDrainLimitNs.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait_sleep(bar, parity, 100000u))
+    if (globaltimer() - t0 > kDrainLimitNs) return;
+}
+
+// A GEMM of U units is spread over Ge = min(G, U) CTAs, CTA c < Ge owning
+// units [c*U/Ge, (c+1)*U/Ge) (never empty); CTAs c >= Ge own none.  So the
+// CTAs that share a tile are consecutive and each holds part of it.
+__device__ __forceinline__ int spread(int total, int G) { return total < G ? total : G; }
+
+// floor(a * b / d) for 0 <= a, b, d < 2^31; 32-bit arithmetic when the
+// product fits (a 64-bit division is a long instruction sequence).
+__device__ __forceinline__ int muldiv(int a, int b, int d) {
+  const unsigned long long prod = (unsigned long long)a * (unsigned)b;
+  if (prod <= 0xFFFFFFFFull) return (int)((uint32_t)prod / (uint32_t)d);
+  return (int)(prod / (unsigned)d);
+}
+
 __device__ __forceinline__ int unit_begin(int c, int total, int G) {
-  return (int)((long long)c * total / G);
+  const int Ge = spread(total, G);
+  return c >= Ge ? total : muldiv(c, total, Ge);
 }
 
 __device__ __forceinline__ int cta_of_unit(int u, int total, int G) {
-  int c = (int)((long long)u * G / total);
-  while (c + 1 < G && unit_begin(c + 1, total, G) <= u) ++c;
+  const int Ge = spread(total, G);
+  int c = muldiv(u, Ge, total);
+  while (c + 1 < Ge && unit_begin(c + 1, total, G) <= u) ++c;
   while (c > 0 && unit_begin(c, total, G) > u) --c;
   return c;
 }
@@ -142,14 +252,36 @@ struct Ring {
   }
 };
 
-// Walks a CTA's range of (tile, stage) units without per-unit division.
-struct UnitIter {
-  int tile, kst, ks;
-  __device__ __forceinline__ UnitIter(int u, int ks_) : ks(ks_) {
-    tile = u / ks_;
-    kst = u - tile * ks_;
+// Walks a CTA's units across the entries of a launch: for each entry the CTA
+// owns units [c*U/G, (c+1)*U/G) of its U = tiles * ks (tile-major).
+struct Walk {
+  const GemmEntry* E;
+  int nE, G, c;
+  int e, u, ub, ue, tile, kst, ks;
+  __device__ __forceinline__ Walk(const GemmEntry* E_, int nE_, int G_, int c_)
+      : E(E_), nE(nE_), G(G_), c(c_) {
+    enter(0);
   }
+  __device__ __forceinline__ void enter(int e0) {
+    for (e = e0; e < nE; ++e) {
+      const int U = E[e].units;
+      ub = unit_begin(c, U, G);
+      ue = unit_begin(c + 1, U, G);
+      if (ub < ue) {
+        u = ub;
+        ks = E[e].ks;
+        tile = u / ks;
+        kst = u - tile * ks;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ bool valid() const { return e < nE; }
   __device__ __forceinline__ void next() {
+    if (++u == ue) {
+      enter(e + 1);
+      return;
+    }
     if (++kst == ks) {
       kst = 0;
       ++tile;
@@ -157,16 +289,32 @@ struct UnitIter {
   }
 };
 
-// int4: 64 codes (group j of the row's 128-byte stage line) to exact bf16
-// pairs (code - zero) in natural k order: a[i] holds k = 2i (low half) and
-// 2i+1 (high half).  Code layout: nibble p (0..7, from the least significant
-// end) of each little-endian 32-bit word holds k = 8w + 2*(p % 4) + p / 4, so
-// the pairs (k0, k1), (k2, k3), (k4, k5), (k6, k7) sit at bit offsets 0, 4, 8
-// and 12 of both 16-bit halves.  Shifted to offset 0 and merged under the
-// bf16 exponent of 128, a nibble c becomes 128 + c exactly (bf16 keeps 7
-// fraction bits); subtracting 128 + zero leaves the exact integer.
-// The line was written by TMA with the 128-byte swizzle: 16-byte chunk c of
-// row m sits at chunk position c ^ (m & 7).
+// Counts a CTA's units across the entries (entry index only), for roles
+// that need no tile coordinates.
+struct Count {
+  const GemmEntry* E;
+  int nE, G, c;
+  int e, rem;
+  __device__ __forceinline__ Count(const GemmEntry* E_, int nE_, int G_, int c_)
+      : E(E_), nE(nE_), G(G_), c(c_) {
+    enter(0);
+  }
+  __device__ __forceinline__ void enter(int e0) {
+    for (e = e0; e < nE; ++e) {
+      const int U = E[e].units;
+      rem = unit_begin(c + 1, U, G) - unit_begin(c, U, G);
+      if (rem > 0) return;
+    }
+  }
+  __device__ __forceinline__ bool valid() const { return e < nE; }
+  __device__ __forceinline__ void next() {
+    if (--rem == 0) enter(e + 1);
+  }
+};
+
+// int4: the 64 codes of group j of a row's 128-byte stage line.  The line was
+// written by TMA with the 128-byte swizzle: 16-byte chunk c of row m sits at
+// chunk position c ^ (m & 7).
 __device__ __forceinline__ void load_w4(uint32_t row_addr, uint32_t m, int j, uint32_t (&words)[8]) {
   const uint32_t sw = m & 7u;
   const uint4 c0 = lds128(row_addr + (((2u * j) ^ sw) << 4));
@@ -175,21 +323,34 @@ __device__ __forceinline__ void load_w4(uint32_t row_addr, uint32_t m, int j, ui
   words[4] = c1.x; words[5] = c1.y; words[6] = c1.z; words[7] = c1.w;
 }
 
-__device__ __forceinline__ void dequant_w4(const uint32_t (&words)[8], uint32_t z, uint32_t (&a)[32]) {
-  const uint32_t zz = (0x4300u | z) * 0x00010001u;             // bf16x2 (128 + z)
+// int4 weights of one 64-k group as fp16 pairs with the group scale folded
+// in: a[i] holds k = 2i (low half) and 2i+1 (high half).  Code layout: nibble
+// p (0..7, from the least significant end) of each little-endian 32-bit word
+// holds k = 8w + 2*(p % 4) + p / 4, so the pairs (k0, k1), (k2, k3), (k4, k5),
+// (k6, k7) sit at bits 0, 4, 8 and 12 of both 16-bit halves.  Merged under
+// the fp16 exponent of 1024 (10 fraction bits), a nibble at bits 0-3 gives
+// 1024 + c and one at bits 4-7 gives 1024 + 16 c, both exact, so the pairs
+// (k2, k3) and (k6, k7) need no shift: they carry a factor 16, which the
+// activations of those k (k % 8 in {2, 3, 6, 7}) take off.  Subtracting
+// 1024 + z (or 1024 + 16 z) is exact; the product with the scale is rounded
+// once to fp16.
+__device__ __forceinline__ void dequant_w4_f16(const uint32_t (&q)[8], uint32_t z, uint32_t s2,
+                                               uint32_t (&a)[32]) {
+  const uint32_t zl = (0x6400u | z) * 0x00010001u;           // (1024 + z) x2
+  const uint32_t zh = (0x6400u | (z << 4)) * 0x00010001u;    // (1024 + 16 z) x2
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const uint32_t q = words[w];
-#pragma unroll
-    for (int o = 0; o < 4; ++o)
-      a[4 * w + o] = sub_bf16x2(lop3_and_or(q >> (4 * o), 0x000F000Fu, 0x43004300u), zz);
+    const uint32_t q8 = q[w] >> 8;
+    a[4 * w + 0] = mul_f16x2(sub_f16x2(lop3_and_or(q[w], 0x000F000Fu, 0x64006400u), zl), s2);
+    a[4 * w + 1] = mul_f16x2(sub_f16x2(lop3_and_or(q[w], 0x00F000F0u, 0x64006400u), zh), s2);
+    a[4 * w + 2] = mul_f16x2(sub_f16x2(lop3_and_or(q8, 0x000F000Fu, 0x64006400u), zl), s2);
+    a[4 * w + 3] = mul_f16x2(sub_f16x2(lop3_and_or(q8, 0x00F000F0u, 0x64006400u), zh), s2);
   }
 }
 
-// int8: 64 codes (group j of the row's 128-byte stage line, 128-byte swizzle
-// as above) to exact bf16.  A biased byte b = code + 128 becomes the fp32
-// 2^23 + b, minus 2^23 + 128 gives the code exactly, and |code| <= 127 fits
-// bf16's 8-bit significand.
+// int8: the 64 codes of group j (128-byte swizzle as above) as exact bf16.
+// A biased byte b = code + 128 becomes the fp32 2^23 + b, minus 2^23 + 128
+// gives the code exactly, and |code| <= 127 fits bf16's 8-bit significand.
 __device__ __forceinline__ void dequant_w8(uint32_t row_addr, uint32_t m, int j, uint32_t (&a)[32]) {
   const uint32_t sw = m & 7u;
   const uint64_t bias = pack_f32x2(0x4B000080u, 0x4B000080u);  // (2^23 + 128) x 2
@@ -212,459 +373,640 @@ __device__ __forceinline__ void dequant_w8(uint32_t row_addr, uint32_t m, int j,
   }
 }
 
+// int8 with a group scale: code * scale rounded once to fp16.  A biased byte
+// b = code + 128 under the fp16 exponent of 1024 is 1024 + b; minus 1152
+// gives the code exactly.
+__device__ __forceinline__ void dequant_w8_f16(uint32_t row_addr, uint32_t m, int j, uint32_t s2,
+                                               uint32_t (&a)[32]) {
+  const uint32_t sw = m & 7u;
+  const uint32_t bias = 0x64806480u;                             // (1024 + 128) x2
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = lds128(row_addr + (((uint32_t)(4 * j + c) ^ sw) << 4));
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t u = words[w] ^ 0x80808080u;
+      a[8 * c + 2 * w] = mul_f16x2(sub_f16x2(__byte_perm(u, 0x6464u, 0x5140u), bias), s2);
+      a[8 * c + 2 * w + 1] = mul_f16x2(sub_f16x2(__byte_perm(u, 0x6464u, 0x5342u), bias), s2);
+    }
+  }
+}
+
+// One 16-byte chunk (8 consecutive k of one activation row, starting at a
+// multiple of 8) from bf16 to the fp16 operand; with `nib` the elements
+// k % 8 in {2, 3, 6, 7} (words 1 and 3) are divided by 16.
+__device__ __forceinline__ uint4 chunk_bf16_to_f16(uint4 v, bool nib) {
+  const float d = nib ? 0.0625f : 1.f;
+  auto cv = [](uint32_t w, float f) {
+    return pack_f16x2(__uint_as_float(w << 16) * f, __uint_as_float(w & 0xFFFF0000u) * f);
+  };
+  return make_uint4(cv(v.x, 1.f), cv(v.y, d), cv(v.z, 1.f), cv(v.w, d));
+}
+
+// The fields of a GEMM the workers' epilogue needs, held in registers while
+// the walk stays in that GEMM (stores to the output could alias the entry as
+// far as the compiler knows, so reading them from the entry each time would
+// reload them after every store).
+struct EpiEntry {
+  void* y;
+  const uint16_t* chscale;
+  int e, N, T, y_f32, pair, per_channel;
+  // a CTA's range holds at most two tiles that other CTAs share (its first
+  // and its last); their first and last contributors, found once per GEMM
+  int tile_a, first_a, last_a, tile_b, first_b, last_b;
+};
+
+// End of a worker's segment of a tile: v holds its rows m, accumulator
+// columns c0.. of the CTA's share of the tile.  A whole tile is written out;
+// a split tile is summed into its fp32 slot and finished by the last
+// contributor to arrive.
 template <int QUANT, int TPAD>
-__global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
-    qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
-                 const __grid_constant__ CUtensorMap tm_scales,
-                 const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
+__device__ __forceinline__ void finish_segment(const EpiEntry& en, const Walk& we, bool seg_from0,
+                                            float (&v)[Cfg<QUANT, TPAD>::kCols], const Params& p,
+                                            int m, int c0, int wk, int lane) {
+  constexpr int kCols = Cfg<QUANT, TPAD>::kCols;
+  const int tile = we.tile;
+  const int row = tile * kTileM + m;
+  const bool whole = seg_from0 && we.kst == we.ks - 1;
+  if (en.per_channel) {
+    const float osc = row < en.N ? __half2float(__ushort_as_half(en.chscale[row])) : 1.f;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) v[c] *= osc;
+  }
+  bool finished = whole;
+  if (!whole) {
+    // split tile: add this warp's part into the tile's fp32 slot (keyed by
+    // the entry and the tile's first contributor, unique among the split
+    // tiles in flight); the last contributor to arrive finishes it
+    const bool a = tile == en.tile_a;
+    const int c_first = a ? en.first_a : en.first_b;
+    const int c_last = a ? en.last_a : en.last_b;
+    const size_t key = (size_t)(en.e % kSplitKeys) * p.slot_ctas + c_first;
+    float* slot = p.partials + (key * kTileM + m) * TPAD + c0;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 4) red_add_f32x4(slot + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+    __syncwarp();
+    int* cnt = p.split_cnt + key * kGemmWorkers + wk;
+    int last = 0;
+    if (lane == 0) last = atomic_add_acq_rel_gpu(cnt, 1) == c_last - c_first;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();   // orders lane 0's acquire before the other lanes' reads
+    if (last) {
+#pragma unroll
+      for (int c = 0; c < kCols; c += 4) {
+        const float4 s4 = ldcg_f32x4(slot + c);
+        v[c] = s4.x;
+        v[c + 1] = s4.y;
+        v[c + 2] = s4.z;
+        v[c + 3] = s4.w;
+      }
+#pragma unroll
+      for (int c = 0; c < kCols; c += 4)
+        __stcg(reinterpret_cast<float4*>(slot + c), make_float4(0.f, 0.f, 0.f, 0.f));
+      if (lane == 0) __stcg(cnt, 0);
+      finished = true;
+    }
+  }
+  if (finished) {
+    if (row < en.N) {
+      // a rotated bf16 GEMM's columns come in (rounded, remainder) pairs per token
+      const int pair = en.pair;
+      const int N = en.N, T = en.T;
+      if (en.y_f32) {
+        float* y = reinterpret_cast<float*>(en.y) + row;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          if (pair && (c & 1)) continue;
+          const int t = (c0 + c) >> pair;
+          const float out = pair ? v[c] + v[c + 1 < kCols ? c + 1 : c] : v[c];
+          if (t < T) y[(size_t)t * N] = out;
+        }
+      } else {
+        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(en.y) + row;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          if (pair && (c & 1)) continue;
+          const int t = (c0 + c) >> pair;
+          const float out = pair ? v[c] + v[c + 1 < kCols ? c + 1 : c] : v[c];
+          if (t < T) y[(size_t)t * N] = __float2bfloat16_rn(out);
+        }
+      }
+    }
+    if (p.gate) {
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(&p.done[en.e], 1);
+    }
+  }
+}
+
+template <int QUANT, int TPAD>
+__global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
+    qgemm_kernel(const __grid_constant__ GemmEntry e0, const Params p) {
   using C = Cfg<QUANT, TPAD>;
-  constexpr int S = C::kStages, NA = C::kNumA, SUB = C::kSub, ND = C::kNumD;
-  constexpr int kMmaWarps = C::kMmaWarps;
+  constexpr int SW = C::kWSlots, SX = C::kXSlots, NA = C::kNA, SUB = C::kSub;
+  constexpr int kCols = C::kCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* ctrl = smem + S * C::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + S;
-  uint64_t* a_full = empty + S;
-  uint64_t* a_empty = a_full + NA;
-  uint64_t* d_full = a_empty + NA;
-  uint64_t* d_empty = d_full + ND;
-  uint64_t* x_full = d_empty + ND;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + S);
+  uint8_t* xreg = smem;
+  uint8_t* wreg = smem + SX * C::kXSlot;
+  uint8_t* ctrl = wreg + SW * C::kWSlot;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* wempty = wfull + SW;
+  uint64_t* xfull = wempty + SW;
+  uint64_t* afull = xfull + SX;
+  // mdone[u % kDM]: every MMA warp has committed stage u (its A slot and
+  // activation slot may be reused once its MMAs complete)
+  uint64_t* mdone = afull + NA;
+  uint64_t* sfull = mdone + C::kDM;
+  uint64_t* sempty = sfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  const GemmEntry* E = p.entries ? p.entries : &e0;
+  const int nE = p.entries ? p.n_entries : 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  const int begin = unit_begin(blockIdx.x, p.total, G);
-  const int end = unit_begin(blockIdx.x + 1, p.total, G);
-  const bool per_channel = (QUANT == kW8) && p.group_size == 0;
+  const int cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&x_full[s], 1);
-      // released by the dequant warps and by the epilogue warps once the
-      // stage's MMAs have completed (they read the stage's scales)
-      mbar_init(&empty[s], C::kDqWarps + 4);
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], kGemmWorkers);
     }
-    for (int s = 0; s < NA; ++s) {
-      mbar_init(&a_full[s], C::kDqWarps);
-      mbar_init(&a_empty[s], kMmaWarps);
-    }
-    for (int b = 0; b < ND; ++b) {
-      mbar_init(&d_full[b], kMmaWarps);
-      mbar_init(&d_empty[b], 4);
+    for (int s = 0; s < SX; ++s) mbar_init(&xfull[s], 1);
+    for (int s = 0; s < NA; ++s) mbar_init(&afull[s], kGemmWorkers);
+    for (int s = 0; s < C::kDM; ++s) mbar_init(&mdone[s], C::kMmaW);   // one commit per MMA warp
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sfull[s], C::kMmaW);
+      mbar_init(&sempty[s], kGemmWorkers);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tensormap(&tm_x);
-      prefetch_tensormap(&tm_codes);
-      prefetch_tensormap(&tm_scales);
-      if (QUANT == kW4) prefetch_tensormap(&tm_zeros);
-    }
-    __syncwarp();
+  if (warp == C::kAlloc) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  if (warp == C::kWProd && lane == 0) {
+    prefetch_tensormap(&E[0].tm_codes);
+    if (E[0].scale_rows) prefetch_tensormap(&E[0].tm_scales);
+    if (QUANT == kW4) prefetch_tensormap(&E[0].tm_zeros);
+  }
+  if (warp == C::kXProd && lane == 0) prefetch_tensormap(&E[0].tm_x);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   pdl_launch_dependents();
 
-  const int nunits = end - begin;
-  // valid 64-k groups of stage kst (only a tile's last stage may be partial)
-  auto nsub_of = [&](int kst) { return kst == p.ks - 1 ? p.last_nsub : SUB; };
+  const Ctl ctl{abort_flag, p.abort_all, p.err, p.wait_ns};
 
-  if (warp == 0) {
+  if (warp == C::kWProd) {
     // ------------------------------------------------------------ weight producer
-    // (the whole warp walks the ring; lane 0 issues the copies)
-    const uint64_t pol_w = policy_evict_first();
-    UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    int n = 0;
-    for (; n < nunits; ++n, it.next(), st_ring.next()) {
-      const int s = st_ring.slot;
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err))) break;
-      if (lane == 0) {
-        uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], p.tx_w);
-        tma_load_2d_hint(st + C::kCodeOff, &tm_codes, &full[s], it.kst * 128, it.tile * kTileM, pol_w);
-        const int g0 = p.group_size ? (it.kst * C::kStageKK) >> p.gshift : 0;
-        tma_load_2d(st + C::kScaleOff, &tm_scales, &full[s], it.tile * kTileM, g0);
-        if (QUANT == kW4) tma_load_2d(st + C::kZeroOff, &tm_zeros, &full[s], it.tile * (kTileM / 2), g0);
+    // (the whole warp walks; one elected lane issues)
+    const bool leader = elect_one();
+    const uint64_t pol = policy_evict_first();
+    // a GEMM's tensor maps and stage sizes, cached while the walk stays in it
+    struct Src {
+      int e = -1;
+      const CUtensorMap *codes, *scales, *zeros;
+      uint32_t tx;
+      int rows, gshift;
+      __device__ __forceinline__ void at(const GemmEntry* E, int e_) {
+        if (e_ == e) return;
+        e = e_;
+        codes = &E[e].tm_codes;
+        scales = &E[e].tm_scales;
+        zeros = &E[e].tm_zeros;
+        tx = E[e].tx_w;
+        rows = E[e].scale_rows;
+        gshift = E[e].gshift;
+      }
+    };
+    Walk w(E, nE, G, cta);
+    Walk pf(E, nE, G, cta);
+    Src sw, spf;
+    int pf_n = 0;
+    Ring<SW> r;
+    int n = 0, skipped = -1;
+    auto prefetch_next = [&]() {
+      spf.at(E, pf.e);
+      if (leader) {
+        tma_prefetch_2d(spf.codes, pf.kst * 128, pf.tile * kTileM);
+        if (spf.rows) {
+          const int g0 = (pf.kst * C::kStageKK) >> spf.gshift;
+          tma_prefetch_2d(spf.scales, pf.tile * kTileM, g0);
+          if (QUANT == kW4) tma_prefetch_2d(spf.zeros, pf.tile * (kTileM / 2), g0);
+        }
+      }
+      pf.next();
+      ++pf_n;
+    };
+    for (; w.valid(); w.next(), r.next(), ++n) {
+      while (pf.valid() && pf_n < n + p.pf_dist) prefetch_next();
+      if (!__all_sync(0xffffffffu, mbar_test_wait(&wempty[r.slot], r.phase ^ 1))) {
+        // the ring is full: run the L2 stream further ahead meanwhile
+        while (pf.valid() && pf_n < n + p.pf_max &&
+               !__all_sync(0xffffffffu, mbar_test_wait(&wempty[r.slot], r.phase ^ 1)))
+          prefetch_next();
+        if (!wait_warp(&wempty[r.slot], r.phase ^ 1, ctl, 512)) break;
+      }
+      if (n == p.skip_unit && cta == 0) {
+        skipped = n;   // test hook: this stage's weights never arrive
+        continue;
+      }
+      sw.at(E, w.e);
+      if (leader) {
+        uint8_t* st = wreg + r.slot * C::kWSlot;
+        mbar_arrive_expect_tx(&wfull[r.slot], sw.tx);
+        tma_load_2d_hint(st, sw.codes, &wfull[r.slot], w.kst * 128, w.tile * kTileM, pol);
+        if (sw.rows) {
+          const int g0 = (w.kst * C::kStageKK) >> sw.gshift;
+          tma_load_2d_hint(st + C::kScaleOff, sw.scales, &wfull[r.slot], w.tile * kTileM, g0, pol);
+          if (QUANT == kW4)
+            tma_load_2d_hint(st + C::kZeroOff, sw.zeros, &wfull[r.slot], w.tile * (kTileM / 2), g0, pol);
+        }
       }
       __syncwarp();
     }
-    if (*abort_flag && lane == 0) {
-      // drain copies still in flight into this CTA's shared memory
-      for (int j = (n > S ? n - S : 0); j < n; ++j) {
-        volatile int no_abort = 0;
-        mbar_wait(&full[j % S], (j / S) & 1, &no_abort, nullptr, kDrainLimitNs);
-      }
+    if (*abort_flag && leader) {
+      // copies still in flight into this CTA's shared memory land before it exits
+      for (int j = (n > SW ? n - SW : 0); j < n; ++j)
+        if (j != skipped) drain_bar(&wfull[j % SW], (uint32_t)((j / SW) & 1));
     }
-  } else if (warp < C::kMmaWarp0) {
-    // ------------------------------------------------------------ dequant
-    const int dq = warp - C::kDqWarp0;
-    const int q = warp & 3;                   // TMEM lane quadrant this warp may access
-    const int j0 = (dq >> 2) * C::kGroupsPerDq;   // first 64-k group of a stage this warp handles
-    const int m = q * 32 + lane;              // weight row inside the tile
-    const uint32_t a_addr0 = tbase + ((uint32_t)(q * 32) << 16) + j0 * 32;
-    const uint32_t row_off = C::kCodeOff + m * 128;
-    const uint32_t zshift = (m & 1) * 4;
-    uint32_t zero_off[C::kGroupsPerDq];
-#pragma unroll
-    for (int i = 0; i < C::kGroupsPerDq; ++i)
-      zero_off[i] = C::kZeroOff + ((64 * (j0 + i)) >> p.gsh) * 64 + (m >> 1);
-    UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    Ring<NA> a_ring;
-    Ring<ND> dprev;   // partial slot of stage n - NA (whose MMAs free this stage's A slot)
-    for (int n = 0; n < nunits; ++n, it.next(), st_ring.next(), a_ring.next()) {
-      const int nsub = nsub_of(it.kst);
-      const int s = st_ring.slot;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err))) break;
-      const uint8_t* st = smem + s * C::kStageBytes;
-      const int sa = a_ring.slot;
-      bool ok = true;
-      // all of this stage's shared-memory reads first (one exposed latency),
-      // then one group at a time: dequantise into registers, store to TMEM
-      // (the first store waits for the A slot to be free; one wait for both)
-      uint32_t words[C::kGroupsPerDq][8];
-      uint32_t zb[C::kGroupsPerDq];
-      if constexpr (QUANT == kW4) {
-#pragma unroll
-        for (int i = 0; i < C::kGroupsPerDq; ++i) {
-          if (j0 + i < nsub) {
-            load_w4(smem_u32(st) + row_off, m, j0 + i, words[i]);
-            zb[i] = st[zero_off[i]];
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < C::kGroupsPerDq; ++i) {
-        const int j = j0 + i;
-        uint32_t a[32];
-        if (j < nsub) {
-          if constexpr (QUANT == kW4) {
-            dequant_w4(words[i], (zb[i] >> zshift) & 0xFu, a);
-          } else {
-            dequant_w8(smem_u32(st) + row_off, m, j, a);
-          }
-        }
-        if (i == 0) {
-          if constexpr (C::kAFromD) {
-            if (n >= NA) {
-              ok = __all_sync(0xffffffffu, mbar_wait(&d_full[dprev.slot], dprev.phase, abort_flag, p.err));
-              dprev.next();
-            }
-          } else {
-            ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], a_ring.phase ^ 1, abort_flag, p.err));
-          }
-          if (!ok) break;
-          tc_fence_after();
-        }
-        if (j < nsub) tmem_st_32x32b_x32(a_addr0 + sa * C::kACols + i * 32, a);
-      }
-      if (!ok) break;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&a_full[sa]);
-        mbar_arrive(&empty[s]);
-      }
-    }
-  } else if (warp < C::kEpWarp0) {
-    // ------------------------------------------------------------ MMA issue
-    // (the whole warp walks the rings; lane 0 issues the MMAs and commits)
-    const int jg = warp - C::kMmaWarp0;       // the 64-k group of each stage this warp issues
-    constexpr uint32_t idesc = idesc_bf16_f32(128, TPAD);
-    UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    Ring<NA> a_ring;
-    Ring<ND> d_ring;
-    int last_sa = -1;
-    uint32_t last_phase = 0;
-    for (int n = 0; n < nunits; ++n, it.next(), st_ring.next(), a_ring.next(), d_ring.next()) {
-      const int s = st_ring.slot, sa = a_ring.slot, b = d_ring.slot;
-      if (!__all_sync(0xffffffffu, mbar_wait(&d_empty[b], d_ring.phase ^ 1, abort_flag, p.err))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&a_full[sa], a_ring.phase, abort_flag, p.err))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&x_full[s], st_ring.phase, abort_flag, p.err))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        if (jg < nsub_of(it.kst)) {
-          const uint32_t d_col = tbase + C::kD0 + b * C::kDCols + jg * TPAD;
-          const uint32_t a_col = tbase + sa * C::kACols + jg * 32;
-          const uint64_t bdesc =
-              smem_desc_sw128(smem + s * C::kStageBytes + C::kXOff) + (uint64_t)((jg * C::kXBoxBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A: 8 TMEM columns (16 bf16) per K16 step; B: +32 bytes inside the swizzled row.
-            mma_ts(d_col, a_col + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
-          }
-        }
-        if constexpr (!C::kAFromD) mma_commit(&a_empty[sa]);
-        mma_commit(&d_full[b]);
-      }
-      __syncwarp();
-      last_sa = b;
-      last_phase = d_ring.phase;
-    }
-    if (*abort_flag && last_sa >= 0 && lane == 0) {
-      // wait for this warp's own MMAs before the CTA frees its tensor memory
-      volatile int no_abort = 0;
-      mbar_wait(&d_full[last_sa], last_phase, &no_abort, nullptr, kDrainLimitNs);
-    }
-  } else if (warp < C::kXWarp) {
-    // ------------------------------------------------------------ epilogue
-    // outputs and split-tile sums may be read or cleared by the previous kernel
+  } else if (warp == C::kXProd) {
+    // ------------------------------------------------------------ activation producer
+    // activations (and the rotation's scratch) may be written by the previous kernel
     pdl_wait_prior();
-    const int q = warp & 3;
-    const int m = q * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    constexpr int kW = TPAD < 32 ? TPAD : (TPAD > 32 ? 16 : 32);   // columns read per wait (register budget)
-
-    float acc[TPAD];
-#pragma unroll
-    for (int t = 0; t < TPAD; ++t) acc[t] = 0.f;
-
-    UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    Ring<ND> d_ring;
+    const bool leader = elect_one();
+    Ring<SX> r;
+    Ring<C::kDM> rdone;     // stage whose MMAs free the slot: n - SX
+    int n = 0, verified = 0;
     bool ok = true;
-    int n = 0;
-    while (ok && n < nunits) {
-      const int tile = it.tile;
-      const int tile_first = tile * p.ks;
-      const int u0 = begin + n;
-      const int seg_end = min(end, tile_first + p.ks);
-      const bool whole_tile = (u0 == tile_first) && (seg_end == tile_first + p.ks);
-      const int nrow = tile * kTileM + m;
-      for (int u = u0; u < seg_end; ++u, ++n, it.next(), st_ring.next(), d_ring.next()) {
-        const int nsub = nsub_of(it.kst);
-        // this stage's group scales (fp32, exact), read while its slot is still held
-        const int s = st_ring.slot;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[s], st_ring.phase, abort_flag, p.err));
+    for (int e = 0; e < nE && ok; ++e) {
+      const GemmEntry& en = E[e];
+      const int ub = unit_begin(cta, en.units, G), ue = unit_begin(cta + 1, en.units, G);
+      const bool gate = p.gate && en.wait_prev && e > 0;
+      if (gate && (en.prep || ub < ue)) {
+        // this GEMM reads what the earlier ones wrote: wait until every one
+        // of their tiles is finished
+        while (verified < e) {
+          if (!__all_sync(0xffffffffu, wait_count(&p.done[verified], kGemmWorkers * E[verified].tiles, ctl))) {
+            ok = false;
+            break;
+          }
+          ++verified;
+        }
         if (!ok) break;
-        float sc[SUB];
-        {
-          const __half* srow = reinterpret_cast<const __half*>(smem + s * C::kStageBytes + C::kScaleOff) + m;
+      }
+      if (en.prep) {
+        // this CTA's share of the activations in the MMA's operand form,
+        // written into the scratch copy, then published
+        const int K = en.K, kind = en.kind;
+        const uint16_t* x = en.x;
+        uint16_t* xp = en.xprep;
+        if (en.prep == 1) {
+          // rotation: one warp per (row, block)
+          const int B = en.rot_block;
+          const int8_t* signs = en.signs;
+          const float rscale = en.rot_scale;
+          const int nblk = K / B;
+          const int pairs = en.T * nblk;
+          for (int pp = cta; pp < pairs; pp += G) {
+            const int t = pp / nblk, b = pp - t * nblk;
+            const size_t col = (size_t)b * B;
+            const uint16_t* xs = x + (size_t)t * K + col;
+            if (kind == kGemmBf16) {
+              // bf16 operands: row t as two rows, 2t (rounded) and 2t+1 (remainder)
+              fwht_warp_any<kFwhtBf16Split>(B, xs, xp + (size_t)(2 * t) * K + col, signs + col, rscale,
+                                            lane, (size_t)K);
+            } else if (kind == kGemmF16Nib) {
+              fwht_warp_any<kFwhtF16Nib>(B, xs, xp + (size_t)t * K + col, signs + col, rscale, lane);
+            } else {
+              fwht_warp_any<kFwhtF16>(B, xs, xp + (size_t)t * K + col, signs + col, rscale, lane);
+            }
+          }
+        } else {
+          // conversion to fp16: 16-byte chunks of 8 consecutive k spread
+          // over every lane of every CTA
+          const bool nib = kind == kGemmF16Nib;
+          const int chunks = en.T * (K / 8);
+          for (int i = cta * 32 + lane; i < chunks; i += G * 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
+            *reinterpret_cast<uint4*>(xp + (size_t)i * 8) = chunk_bf16_to_f16(v, nib);
+          }
+        }
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(&p.rot_done[e], 1);
+      }
+      if (ub >= ue) continue;
+      if (en.prep && !__all_sync(0xffffffffu, wait_count(&p.rot_done[e], G, ctl))) {
+        ok = false;
+        break;
+      }
+      if (gate || en.prep) fence_proxy_async_global();
+      if (lane == 0) prefetch_tensormap(&en.tm_x);
+      const CUtensorMap* tmx = &en.tm_x;
+      const int ks = en.ks;
+      int kst = ub % ks;
+      for (int u = ub; u < ue; ++u, r.next(), ++n) {
+        if (n >= SX) {
+          if (!wait_warp(&mdone[rdone.slot], rdone.phase, ctl, 512)) {
+            ok = false;
+            break;
+          }
+          rdone.next();
+        }
+        if (leader) {
+          uint8_t* st = xreg + r.slot * C::kXSlot;
+          mbar_arrive_expect_tx(&xfull[r.slot], (uint32_t)(SUB * C::kXBox));
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
-            sc[j] = per_channel ? 1.f : __half2float(srow[((64 * j) >> p.gsh) * kTileM]);
+            tma_load_2d(st + j * C::kXBox, tmx, &xfull[r.slot], kst * C::kStageKK + kGroupK * j, 0);
         }
-        // this stage's partials; once they are complete the stage's MMAs have
-        // finished reading its activations, so the slot can be released
-        const int b = d_ring.slot;
-        ok = __all_sync(0xffffffffu, mbar_wait(&d_full[b], d_ring.phase, abort_flag, p.err));
-        if (!ok) break;
-        if (lane == 0) mbar_arrive(&empty[s]);
-        tc_fence_after();
-        const uint32_t dbase = tbase + lane_base + C::kD0 + b * C::kDCols;
-#pragma unroll
-        for (int j = 0; j < SUB; ++j) {
-          if (j < nsub) {
-            const uint64_t s2 = pack_f32x2(__float_as_uint(sc[j]), __float_as_uint(sc[j]));
-#pragma unroll
-            for (int c0 = 0; c0 < TPAD; c0 += kW) {
-              uint32_t r[kW];
-#pragma unroll
-              for (int h = 0; h < kW / 16; ++h)
-                tmem_ld_32x32b_x16(dbase + j * TPAD + c0 + h * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[h * 16]));
-              tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < kW; c += 2) {
-                // columns (t, t + 1) in one fma.rn.f32x2
-                const uint64_t d = fma_f32x2(s2, pack_f32x2(r[c], r[c + 1]),
-                                             pack_f32x2(__float_as_uint(acc[c0 + c]), __float_as_uint(acc[c0 + c + 1])));
-                acc[c0 + c] = __uint_as_float((uint32_t)d);
-                acc[c0 + c + 1] = __uint_as_float((uint32_t)(d >> 32));
-              }
-            }
-          }
-        }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&d_empty[b]);
-      }
-      if (!ok) break;
-
-      float v[TPAD];
-      const float osc = per_channel && nrow < p.N ? __half2float(__ushort_as_half(p.scales[nrow])) : 1.f;
-#pragma unroll
-      for (int t = 0; t < TPAD; ++t) {
-        v[t] = acc[t] * osc;
-        acc[t] = 0.f;
-      }
-      if (whole_tile) {
-        if (nrow < p.N) {
-#pragma unroll
-          for (int t = 0; t < TPAD; ++t) {
-            if (t < p.T) {
-              if (p.y_f32)
-                reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = v[t];
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(v[t]);
-            }
-          }
-        }
-      } else {
-        // Split tile: add this warp's 32 rows of the CTA's partial into the
-        // tile's fp32 slot (keyed by the tile's first contributor, unique per
-        // split tile).  Arrivals are counted per lane quadrant, so each warp
-        // finishes its own rows: the last to arrive converts the sum and
-        // clears the slot, with no barrier between the epilogue warps.
-        const int c_first = cta_of_unit(tile_first, p.total, G);
-        const int c_last = cta_of_unit(tile_first + p.ks - 1, p.total, G);
-        // slot layout [128 rows][TPAD]: a thread's values are contiguous, so
-        // the sums travel as 16-byte vector reductions and loads
-        float* slot = p.partials + (size_t)c_first * kPartialSlotFloats + (size_t)m * TPAD;
-#pragma unroll
-        for (int t = 0; t < TPAD; t += 4)
-          if (t < p.T) red_add_f32x4(slot + t, v[t], v[t + 1], v[t + 2], v[t + 3]);
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomic_add_acq_rel_gpu(&p.counters[tile * 4 + q], 1) == c_last - c_first;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        __syncwarp();   // orders lane 0's acquire before the other lanes' reads
-        if (last) {
-          // every read before any store (one L2 round trip for T <= 32): the
-          // stores may alias the slot as far as the compiler knows
-          constexpr int kB = TPAD % 32 == 0 ? 32 : 16;
-#pragma unroll
-          for (int h = 0; h < TPAD / kB; ++h) {
-            float4 w[kB / 4];
-#pragma unroll
-            for (int c = 0; c < kB / 4; ++c)
-              w[c] = (h * kB + 4 * c < p.T) ? ldcg_f32x4(slot + h * kB + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < kB / 4; ++c) {
-              const int t0 = h * kB + 4 * c;
-              if (t0 < p.T) {
-                __stcg(reinterpret_cast<float4*>(slot + t0), make_float4(0.f, 0.f, 0.f, 0.f));
-                const float wv[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int t = t0 + e;
-                  if (t < p.T && nrow < p.N) {
-                    if (p.y_f32)
-                      reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nrow] = wv[e];
-                    else
-                      reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nrow] = __float2bfloat16_rn(wv[e]);
-                  }
-                }
-              }
-            }
-          }
-          // only this warp touches the counter until the kernel ends
-          if (lane == 0) __stcg(&p.counters[tile * 4 + q], 0);
-        }
+        if (++kst == ks) kst = 0;
       }
     }
-  } else {
-    // ------------------------------------------------------------ activation producer
-    // (the activations may be written by the previous kernel; a slot is
-    // refilled once the epilogue has seen that stage's MMAs complete)
-    pdl_wait_prior();
-    UnitIter it(begin, p.ks);
-    Ring<S> st_ring;
-    int n = 0;
-    for (; n < nunits; ++n, it.next(), st_ring.next()) {
-      const int s = st_ring.slot;
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], st_ring.phase ^ 1, abort_flag, p.err))) break;
-      if (lane == 0) {
-        const int nsub = nsub_of(it.kst);
-        uint8_t* st = smem + s * C::kStageBytes + C::kXOff;
-        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(nsub * C::kXBoxBytes));
-        for (int j = 0; j < nsub; ++j)
-          tma_load_2d(st + j * C::kXBoxBytes, &tm_x, &x_full[s], it.kst * C::kStageKK + 64 * j, 0);
+    if (*abort_flag && leader) {
+      for (int j = (n > SX ? n - SX : 0); j < n; ++j) drain_bar(&xfull[j % SX], (uint32_t)((j / SX) & 1));
+    }
+  } else if (warp < C::kMma0) {
+    // the TMEM owner and the idle warp wait at the final barrier
+  } else if (warp < C::kWorker0) {
+    // ------------------------------------------------------------ MMA issue
+    // warp kMma0 + k issues the K16 MMAs of groups k*kGpm .. into its own
+    // accumulator of the current segment's set (the whole warp walks; one
+    // elected lane issues)
+    const int k = warp - C::kMma0;
+    const bool leader = elect_one();
+    Walk w(E, nE, G, cta);
+    const uint64_t xdesc0 = smem_desc_sw128(xreg);
+    Ring<NA> ra;
+    Ring<SX> rx;
+    Ring<C::kDM> rm;
+    Ring<2> rs;
+    int ce = -1, last_m = -1;
+    uint32_t idesc = 0, last_mph = 0;
+    for (; w.valid(); w.next(), ra.next(), rx.next(), rm.next()) {
+      if (w.e != ce) {
+        ce = w.e;
+        idesc = E[ce].idesc;
+      }
+      const bool seg0 = w.kst == 0 || w.u == w.ub;
+      const bool seg1 = w.kst == w.ks - 1 || w.u == w.ue - 1;
+      // a segment starts on a zeroed accumulator (zeroed at the start of the
+      // launch, then by the workers after they read it)
+      if (seg0 && !wait_warp(&sempty[rs.slot], rs.phase, ctl)) break;
+      if (!wait_warp(&afull[ra.slot], ra.phase, ctl)) break;
+      if (!wait_warp(&xfull[rx.slot], rx.phase, ctl)) break;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t d = tbase + rs.slot * C::kDCols;
+        const uint32_t a0 = tbase + C::kA0 + ra.slot * C::kACols;
+        const uint64_t xd = xdesc0 + (uint64_t)((rx.slot * C::kXSlot) >> 4);
+#pragma unroll
+        for (int gi = 0; gi < C::kGpm; ++gi) {
+          const int g = k * C::kGpm + gi;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 8 TMEM columns (16 elements) per K16 step; B: +32 bytes inside the swizzled row
+            mma_ts(d, a0 + g * 32 + kk * 8, xd + (uint64_t)((g * C::kXBox) >> 4) + kk * 2, idesc, 1u);
+          }
+        }
+        mma_commit(&mdone[rm.slot]);
+        if (seg1) mma_commit(&sfull[rs.slot]);
       }
       __syncwarp();
+      last_m = rm.slot;
+      last_mph = rm.phase;
+      if (seg1) rs.next();
     }
-    if (*abort_flag && lane == 0) {
-      for (int j = (n > S ? n - S : 0); j < n; ++j) {
-        volatile int no_abort = 0;
-        mbar_wait(&x_full[j % S], (j / S) & 1, &no_abort, nullptr, kDrainLimitNs);
+    // the CTA frees its tensor memory and shared memory only after its
+    // MMAs have completed and their commits have arrived
+    if (last_m >= 0 && leader) drain_bar(&mdone[last_m], last_mph);
+  } else {
+    // ------------------------------------------------------------ workers
+    const int wk = warp - C::kWorker0;
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+    const int h = wk >> 2;
+    const int m = q * 32 + lane;                  // weight row inside the tile
+    const int j0 = h * C::kGpw;                   // first 64-k group this warp dequantises
+    const int c0 = h * kCols;                     // first accumulator column this warp reads
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const uint32_t zshift = (m & 1) * 4;
+    const uint32_t wbase = smem_u32(wreg);
+    Count wd(E, nE, G, cta);                      // stage being dequantised (n)
+    Walk we(E, nE, G, cta);                       // stage whose segment may end (n - 1)
+    // per-entry shared-memory offsets inside a weight slot: this row's zero
+    // byte and scale of each dequantised group
+    uint32_t zoff[C::kGpw], soff[C::kGpw];
+    int ed = -1, ee = -1, kind = 0;
+    EpiEntry epi{};
+    auto enter_d = [&](int e) {
+      ed = e;
+      const int gsh = E[e].gsh;
+      kind = E[e].kind;
+#pragma unroll
+      for (int i = 0; i < C::kGpw; ++i) {
+        const int row = (kGroupK * (j0 + i)) >> gsh;
+        zoff[i] = C::kZeroOff + row * 64 + (m >> 1);
+        soff[i] = C::kScaleOff + row * (kTileM * 2) + m * 2;
       }
+    };
+    auto enter_e = [&](int e) {
+      ee = e;
+      const GemmEntry& en = E[e];
+      epi.y = en.y;
+      epi.chscale = en.chscale;
+      epi.e = e;
+      epi.N = en.N;
+      epi.T = en.T;
+      epi.y_f32 = en.y_f32;
+      epi.pair = en.rot_block && en.kind == kGemmBf16 ? 1 : 0;
+      epi.per_channel = en.scale_rows == 0;
+      const int U = en.units, ks = en.ks;
+      const int ub = unit_begin(cta, U, G), ue = unit_begin(cta + 1, U, G);
+      if (ub < ue) {
+        epi.tile_a = ub / ks;
+        epi.first_a = cta_of_unit(epi.tile_a * ks, U, G);
+        epi.last_a = cta_of_unit(epi.tile_a * ks + ks - 1, U, G);
+        epi.tile_b = (ue - 1) / ks;
+        epi.first_b = cta_of_unit(epi.tile_b * ks, U, G);
+        epi.last_b = cta_of_unit(epi.tile_b * ks + ks - 1, U, G);
+      }
+    };
+    Ring<SW> rw;
+    Ring<NA> ra;
+    Ring<C::kDM> rm;        // stage whose MMAs free the A slot: n - NA
+    Ring<2> rs;
+    bool seg_from0 = false, ok = true;
+    // both accumulators start at zero
+#pragma unroll
+    for (int sl = 0; sl < 2; ++sl) tmem_zero_cols<kCols>(tbase + lane_base + sl * C::kDCols + c0);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sempty[0]);
+      mbar_arrive(&sempty[1]);
+    }
+    for (int n = 0;; ++n) {
+      const bool has_d = wd.valid();
+      const bool has_e = n > 0 && we.valid();
+      if (!has_d && !has_e) break;
+      if (has_d) {
+        // ---- dequantise stage n into A slot n % NA
+        if (wd.e != ed) enter_d(wd.e);
+        if (!wait_warp(&wfull[rw.slot], rw.phase, ctl)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = wbase + rw.slot * C::kWSlot;
+        uint32_t words[C::kGpw][8];
+        uint32_t zb[C::kGpw], s2[C::kGpw];
+        if constexpr (QUANT == kW4) {
+#pragma unroll
+          for (int i = 0; i < C::kGpw; ++i) {
+            load_w4(st + m * 128, m, j0 + i, words[i]);
+            zb[i] = (lds_u8(st + zoff[i]) >> zshift) & 0xFu;
+            s2[i] = (uint32_t)lds_u16(st + soff[i]) * 0x00010001u;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::kGpw; ++i) s2[i] = kind == kGemmF16 ? (uint32_t)lds_u16(st + soff[i]) * 0x00010001u : 0u;
+        }
+        // the A slot is free once the MMAs that read it (stage n - NA) have completed
+        if (n >= NA) {
+          if (!wait_warp(&mdone[rm.slot], rm.phase, ctl)) {
+            ok = false;
+            break;
+          }
+          rm.next();
+        }
+        tc_fence_after();
+        const uint32_t aslot = tbase + lane_base + C::kA0 + ra.slot * C::kACols;
+#pragma unroll
+        for (int i = 0; i < C::kGpw; ++i) {
+          uint32_t a[32];
+          if constexpr (QUANT == kW4) {
+            dequant_w4_f16(words[i], zb[i], s2[i], a);
+          } else {
+            if (kind == kGemmF16)
+              dequant_w8_f16(st + m * 128, m, j0 + i, s2[i], a);
+            else
+              dequant_w8(st + m * 128, m, j0 + i, a);
+          }
+          tmem_st_32x32b_x32(aslot + (j0 + i) * 32, a);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[ra.slot]);
+          mbar_arrive(&wempty[rw.slot]);   // codes, scales and zero points read
+        }
+      }
+      if (has_e) {
+        // ---- stage n - 1: the end of a segment reads the accumulators
+        if (n == 1) {
+          // outputs and split-tile sums may still be used by the previous kernel
+          pdl_wait_prior();
+        }
+        if (we.kst == 0 || we.u == we.ub) seg_from0 = we.kst == 0;
+        if (we.kst == we.ks - 1 || we.u == we.ue - 1) {
+          if (we.e != ee) enter_e(we.e);
+          if (!wait_warp(&sfull[rs.slot], rs.phase, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dbase = tbase + lane_base + rs.slot * C::kDCols + c0;
+          float v[kCols];
+          tmem_ld_cols<kCols>(dbase, v);
+          tmem_wait_ld();
+          tmem_zero_cols<kCols>(dbase);     // the next segment on this accumulator adds from zero
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[rs.slot]);
+          rs.next();
+          finish_segment<QUANT, TPAD>(epi, we, seg_from0, v, p, m, c0, wk, lane);
+        }
+        we.next();
+      }
+      if (has_d) {
+        wd.next();
+        rw.next();
+        ra.next();
+      }
+    }
+    if (!ok) {
+      tmem_wait_st();
+      tmem_wait_ld();
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == C::kAlloc) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
+  }
+  if (threadIdx.x == 0 && (p.gate || p.any_prep)) {
+    // the last CTA to leave resets the per-entry counters for the next launch
+    __threadfence();
+    const int old = atomic_add_acq_rel_gpu(p.exit_cnt, 1);
+    if (old == G - 1) {
+      for (int e = 0; e < nE; ++e) {
+        p.done[e] = 0;
+        p.rot_done[e] = 0;
+      }
+      *p.exit_cnt = 0;
+      __threadfence();
+    }
   }
 }
 
 template <int QUANT, int TPAD>
-int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
+int launch_t(spec_ctx* ctx, const GemmEntry& e0, const GemmEntry* dev_entries, int n, int gate,
+             int any_prep, int G, cudaStream_t stream) {
   using C = Cfg<QUANT, TPAD>;
-  CUtensorMap tx, tc, ts, tz;
-  int rc;
-  rc = encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.T,
-                      (uint64_t)a.K * 2, kStageK, TPAD, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc) return rc;
-  const uint64_t row_bytes = QUANT == kW4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
-  rc = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qcodes, row_bytes, (uint64_t)a.N,
-                      row_bytes, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc) return rc;
-  const uint64_t groups = a.group_size ? (uint64_t)(a.K / a.group_size) : 1;
-  const int sr = a.group_size && a.group_size < C::kStageKK ? C::kStageKK / a.group_size : 1;
-  rc = encode_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)a.N, groups,
-                      (uint64_t)a.N * 2, kTileM, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (rc) return rc;
-  if (QUANT == kW4) {
-    rc = encode_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.zeros, (uint64_t)a.N / 2, groups,
-                        (uint64_t)a.N / 2, kTileM / 2, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rc) return rc;
-  } else {
-    tz = ts;
-  }
-
   Params p;
-  p.T = a.T;
-  p.N = a.N;
-  p.K = a.K;
-  p.group_size = a.group_size;
-  p.gshift = 0;
-  while (a.group_size && (1 << p.gshift) < a.group_size) ++p.gshift;
-  p.ks = (a.K + C::kStageKK - 1) / C::kStageKK;
-  p.last_nsub = (a.K - (p.ks - 1) * C::kStageKK) / 64;
-  p.gsh = (a.group_size == 0 || a.group_size > C::kStageKK) ? 31 : p.gshift;
-  const long long tiles = (a.N + kTileM - 1) / kTileM;
-  p.total = tiles * p.ks;
-  p.tx_w = C::kCodeBytes + sr * kTileM * 2 + (QUANT == kW4 ? sr * 64 : 0);
-  p.scales = a.scales;
-  p.y = a.y;
-  p.y_f32 = a.y_f32;
+  p.entries = dev_entries;
+  p.n_entries = n;
+  p.gate = gate;
+  p.any_prep = any_prep;
+  p.slot_ctas = ctx->num_sms;
   p.partials = ctx->partials;
-  p.counters = ctx->tile_counters;
+  p.split_cnt = ctx->split_cnt;
+  p.done = ctx->done;
+  p.rot_done = ctx->rot_done;
+  p.exit_cnt = ctx->exit_cnt;
   p.err = ctx->err;
-  // persistent grid of one CTA per SM with an even share of units each
-  long long G = ctx->num_sms;
-  if (G > p.total) G = p.total;
-  const long long per = (p.total + G - 1) / G;
-  G = (p.total + per - 1) / per;
-  if (G > ctx->max_slots) return set_error(SPEC_ERR_OOM, "workspace has too few partial slots");
+  p.abort_all = ctx->abort_all;
+  p.wait_ns = ctx->test_wait_ns ? ctx->test_wait_ns : kWaitLimitNs;
+  p.skip_unit = ctx->test_skip_unit;
+  p.pf_dist = ctx->pf_dist;
+  p.pf_max = ctx->pf_max;
+  ctx->test_wait_ns = 0;
+  ctx->test_skip_unit = -1;
 
   static std::atomic<uint32_t> attr_done{0};   // per instantiation, one bit per device
   const uint32_t bit = ctx->device < 32 ? (1u << ctx->device) : 0u;
   if (!bit || !(attr_done.load() & bit)) {
-    rc = check_cuda(cudaFuncSetAttribute(qgemm_kernel<QUANT, TPAD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes),
-                    "cudaFuncSetAttribute(qgemm)");
+    int rc = check_cuda(cudaFuncSetAttribute(qgemm_kernel<QUANT, TPAD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+                        "cudaFuncSetAttribute(qgemm)");
     if (rc) return rc;
     attr_done.fetch_or(bit);
   }
-  // programmatic stream serialisation: see the design notes at the top
+  // programmatic stream serialisation: the launch may start while the
+  // previous kernel finishes; every read of its results waits for it
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(C::kThreads);
@@ -675,25 +1017,117 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return check_cuda(cudaLaunchKernelEx(&cfg, qgemm_kernel<QUANT, TPAD>, tx, tc, ts, tz, p), "qgemm launch");
+  return check_cuda(cudaLaunchKernelEx(&cfg, qgemm_kernel<QUANT, TPAD>, e0, p), "qgemm launch");
 }
 
 template <int QUANT>
-int launch_q(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
-  const int tpad = (a.T + 15) / 16 * 16;
+int launch_q(spec_ctx* ctx, int tpad, const GemmEntry& e0, const GemmEntry* dev, int n, int gate,
+             int any_prep, int G, cudaStream_t s) {
   switch (tpad) {
-    case 16: return launch_t<QUANT, 16>(ctx, a, s);
-    case 32: return launch_t<QUANT, 32>(ctx, a, s);
-    case 48: return launch_t<QUANT, 48>(ctx, a, s);
-    case 64: return launch_t<QUANT, 64>(ctx, a, s);
-    default: return set_error(SPEC_ERR_SHAPE, "T=%d outside 1..64", a.T);
+    case 16: return launch_t<QUANT, 16>(ctx, e0, dev, n, gate, any_prep, G, s);
+    case 32: return launch_t<QUANT, 32>(ctx, e0, dev, n, gate, any_prep, G, s);
+    case 48: return launch_t<QUANT, 48>(ctx, e0, dev, n, gate, any_prep, G, s);
+    case 64: return launch_t<QUANT, 64>(ctx, e0, dev, n, gate, any_prep, G, s);
+    default: return set_error(SPEC_ERR_SHAPE, "padded T=%d outside 16..64", tpad);
   }
+}
+
+int stage_k(int quant) { return quant == kW4 ? 256 : 128; }
+
+// The MMA operand form of a GEMM (see GemmKind).
+int kind_of(const GemmArgs& a) {
+  return a.quant == kW4 ? kGemmF16Nib : (a.group_size ? kGemmF16 : kGemmBf16);
 }
 
 }  // namespace
 
+int build_entry(spec_ctx* ctx, const GemmArgs& a, int tpad, int index, GemmEntry* out) {
+  GemmEntry e;
+  std::memset(&e, 0, sizeof(e));
+  const int SK = stage_k(a.quant);
+  const bool rot = a.signs != nullptr;
+  const int kind = kind_of(a);
+  // activations the MMA reads in another form are prepared inside the launch
+  // into the scratch copy of this GEMM's key (a rotated bf16 GEMM's as 2T
+  // rows, (rounded, remainder) per token)
+  const int prep = rot ? 1 : (kind != kGemmBf16 ? 2 : 0);
+  uint16_t* xp = prep ? ctx->xprep + (size_t)(index % kSplitKeys) * kMaxT * kMaxK : nullptr;
+  const uint16_t* xsrc = prep ? xp : a.x;
+  const uint64_t xrows = rot && kind == kGemmBf16 ? 2 * (uint64_t)a.T : (uint64_t)a.T;
+  if ((int)xrows > tpad) return set_error(SPEC_ERR_SHAPE, "internal: padded T %d below %d rows", tpad, (int)xrows);
+  int rc = encode_tmap_2d(&e.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc, (uint64_t)a.K, xrows,
+                          (uint64_t)a.K * 2, kGroupK, tpad, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  const uint64_t row_bytes = a.quant == kW4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+  rc = encode_tmap_2d(&e.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qcodes, row_bytes, (uint64_t)a.N,
+                      row_bytes, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  int sr = 0;
+  if (a.group_size) {
+    const uint64_t groups = (uint64_t)(a.K / a.group_size);
+    sr = a.group_size < SK ? SK / a.group_size : 1;
+    rc = encode_tmap_2d(&e.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)a.N, groups,
+                        (uint64_t)a.N * 2, kTileM, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+    if (a.quant == kW4) {
+      rc = encode_tmap_2d(&e.tm_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.zeros, (uint64_t)a.N / 2, groups,
+                          (uint64_t)a.N / 2, kTileM / 2, sr, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc) return rc;
+    }
+  }
+  e.x = a.x;
+  e.signs = a.signs;
+  e.xprep = xp;
+  e.chscale = a.group_size ? nullptr : a.scales;
+  e.y = a.y;
+  e.T = a.T;
+  e.N = a.N;
+  e.K = a.K;
+  e.rot_block = rot ? a.rot_block : 0;
+  e.rot_scale = rot ? (float)(1.0 / std::sqrt((double)a.rot_block)) : 0.f;
+  e.ks = (a.K + SK - 1) / SK;
+  e.tiles = (a.N + kTileM - 1) / kTileM;
+  e.units = e.ks * e.tiles;
+  e.gshift = 0;
+  while (a.group_size && (1 << e.gshift) < a.group_size) ++e.gshift;
+  e.gsh = (a.group_size == 0 || a.group_size > SK) ? 31 : e.gshift;
+  e.scale_rows = sr;
+  e.tx_w = kTileM * 128 + (uint32_t)sr * kTileM * 2 + (a.quant == kW4 ? (uint32_t)sr * 64 : 0u);
+  e.y_f32 = a.y_f32;
+  e.wait_prev = a.wait_prev;
+  e.kind = kind;
+  e.prep = prep;
+  e.idesc = kind == kGemmBf16 ? idesc_bf16_f32(128, tpad) : idesc_f16_f32(128, tpad);
+  *out = e;
+  return SPEC_OK;
+}
+
+int gemm_tpad(const GemmArgs& a) {
+  const int rows = a.signs && kind_of(a) == kGemmBf16 ? 2 * a.T : a.T;
+  return (rows + 15) / 16 * 16;
+}
+
 int launch_qgemm(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
-  return a.quant == kW4 ? launch_q<kW4>(ctx, a, s) : launch_q<kW8>(ctx, a, s);
+  const int tpad = gemm_tpad(a);
+  GemmEntry e;
+  int rc = build_entry(ctx, a, tpad, 0, &e);
+  if (rc) return rc;
+  // persistent grid of at most one CTA per SM with an even share of units each
+  long long G = ctx->num_sms;
+  if (G > e.units) G = e.units;
+  const long long per = (e.units + G - 1) / G;
+  G = (e.units + per - 1) / per;
+  if (e.prep) G = ctx->num_sms < e.units ? ctx->num_sms : e.units;
+  return a.quant == kW4 ? launch_q<kW4>(ctx, tpad, e, nullptr, 1, 0, e.prep != 0, (int)G, s)
+                        : launch_q<kW8>(ctx, tpad, e, nullptr, 1, 0, e.prep != 0, (int)G, s);
+}
+
+int launch_qgemm_stack(spec_ctx* ctx, const spec_gemm_stack* st, cudaStream_t s) {
+  GemmEntry dummy;
+  std::memset(&dummy, 0, sizeof(dummy));
+  return st->quant == kW4
+             ? launch_q<kW4>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->any_prep, ctx->num_sms, s)
+             : launch_q<kW8>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->any_prep, ctx->num_sms, s);
 }
 
 }  // namespace sv

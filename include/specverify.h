@@ -74,6 +74,8 @@ enum spec_status {
 
 enum spec_dtype { SPEC_DTYPE_BF16 = 0, SPEC_DTYPE_F32 = 1 };
 
+enum spec_quant { SPEC_QUANT_W4 = 0, SPEC_QUANT_W8 = 1 };
+
 /* Library version, (major << 16) | minor. */
 int spec_version(void);
 
@@ -103,10 +105,13 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  *   y[t][n] = sum_k x'[t][k] * (code[n][k] - zero[k/g][n]) * scale[k/g][n]
  * x' = x, or, when signs != NULL and hadamard_block > 0, the block random
  * Hadamard rotation of x (see fwht_rotate; the weights are taken as stored
- * already rotated).
- * Sizes: 1 <= T <= 64; N % 32 == 0; K % 64 == 0; group_size a power of two
- * >= 64 with K % group_size == 0.  y_dtype is SPEC_DTYPE_BF16 or
- * SPEC_DTYPE_F32.
+ * already rotated).  The rotation runs inside the same launch, in fp32, and
+ * its result enters the tensor cores as the sum of two bf16 values (the
+ * rounded value and its remainder), so it adds no bf16 rounding; it uses the
+ * context's rotation scratch.
+ * Sizes: 1 <= T <= 64 (T <= 32 with rotation); N % 32 == 0; K % 64 == 0;
+ * group_size a power of two >= 64 with K % group_size == 0.  y_dtype is
+ * SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
  * Numerics: the tensor cores multiply the exact integers (code - zero),
  * held in bf16, by the bf16 activations as given, and sum each 64-k block in
  * fp32; the block's fp16 scale is then applied in fp32 and the blocks are
@@ -130,6 +135,74 @@ int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, const uint16_t* x, void* y, int y_dtype, int T,
                 int N, int K, const int8_t* signs, int hadamard_block,
                 void* stream);
+
+/* One GEMM of a stack (see qgemm_stack_create).  Fields as the arguments of
+ * qgemm_w4a16 (quant SPEC_QUANT_W4) or qgemm_w8a16 (SPEC_QUANT_W8; zeros is
+ * ignored), plus wait_prev: 1 = this GEMM reads its activations (and writes
+ * its outputs) only after every earlier GEMM of the stack has written all of
+ * its outputs, as if each GEMM were a separate call on one stream; 0 = it
+ * does not depend on the GEMMs before it (for example q, k and v projections
+ * of one input).  The first entry's wait_prev is ignored: the launch itself
+ * follows the previous work on its stream. */
+typedef struct spec_gemm_desc {
+  int quant;
+  const void* qcodes;
+  const uint16_t* scales;
+  const uint8_t* zeros;
+  int group_size;
+  const uint16_t* x;
+  void* y;
+  int y_dtype;
+  int T, N, K;
+  const int8_t* signs;
+  int hadamard_block;
+  int wait_prev;
+} spec_gemm_desc;
+
+typedef struct spec_gemm_stack spec_gemm_stack;
+
+/* A stack of verify GEMMs run by one persistent launch: the weight pass of
+ * the verify step, every projection of every layer in order ("Karpathy's
+ * Trick ...", section "Why batch-one decoding is memory-bound": one pass
+ * streams every weight once, so the pass is bounded by memory bandwidth).
+ * One launch keeps the weight stream running from one GEMM into the next:
+ * a GEMM that waits for its predecessors' outputs (wait_prev) waits on the
+ * device while the weights after it keep streaming in.
+ * qgemm_stack_create checks and records n descriptors (1 <= n <= 1024); the
+ * descriptors' pointers and sizes are fixed from then on (the tensors must
+ * stay allocated while the stack is used).  Rules beyond each GEMM's own:
+ * one quant for all entries; at most 3 consecutive entries (after the
+ * first) with wait_prev = 0; a rotated entry after another rotated entry
+ * needs wait_prev = 1 (rotated GEMMs share the context's rotation scratch).
+ * The stack holds a small device array (cudaMalloc at creation) and belongs
+ * to `ctx`.  qgemm_stack_run enqueues the whole stack on `stream` (one
+ * kernel launch; a launch may be captured in a CUDA graph); the results are
+ * those of calling the GEMMs one by one.  qgemm_stack_destroy frees the
+ * stack (NULL accepted). */
+int qgemm_stack_create(spec_ctx* ctx, const spec_gemm_desc* descs, int n,
+                       spec_gemm_stack** out);
+int qgemm_stack_run(spec_ctx* ctx, const spec_gemm_stack* stack, void* stream);
+int qgemm_stack_destroy(spec_gemm_stack* stack);
+
+/* Tuning of the GEMMs' weight stream on this context: each CTA keeps the L2
+ * prefetch of its upcoming weight boxes `lead` stages ahead of its
+ * shared-memory loads, and up to `lead_when_full` stages ahead while its
+ * shared-memory ring is full (0 <= lead <= lead_when_full <= 256).  Results
+ * do not depend on it.  Defaults 4 and 16 (or the environment variables
+ * SPEC_PREFETCH_LEAD and SPEC_PREFETCH_LEAD_FULL at spec_create). */
+int spec_set_stream_prefetch(spec_ctx* ctx, int lead, int lead_when_full);
+
+/* Test hook for the failure path of the GEMMs' bounded waits (not for
+ * production use): the next GEMM launch on this context (qgemm_w4a16,
+ * qgemm_w8a16 or qgemm_stack_run) gives every wait a limit of
+ * wait_limit_ns (1e5 .. 2e9 ns) instead of the default 2 s, and, when
+ * skip_unit >= 0, its CTA 0 never loads the weights of its skip_unit-th
+ * stage (if it owns that many), so the waits for that stage run out.  The kernel then records
+ * SPEC_ERR_TIMEOUT, stops every CTA, lets its copies and MMAs complete,
+ * frees its tensor memory and returns; spec_sync_status reports the error
+ * and resets the workspace, after which the context is usable again.  The
+ * hook applies to one launch only. */
+int spec_test_stall(spec_ctx* ctx, int skip_unit, uint64_t wait_limit_ns);
 
 /* Block-diagonal random Hadamard rotation ("How Uzu optimizes bytes and tokens
  * per pass": random sign flips applied before the mixing, +1/-1 entries and
@@ -197,9 +270,10 @@ int spec_accept_noalloc(const float* target_logits, const float* draft_probs,
                         int32_t* near_tie_flags, int32_t* device_status,
                         void* stream);
 
-/* Greedy tree acceptance ("Karpathy's Trick ...", section "Issue with parallel
- * draft generation": the main model verifies the tree and accepts the longest
- * valid path; "Local LLM 4x Faster ...": verify the entire tree at once).
+/* Greedy tree acceptance.  Sources: "Karpathy's Trick ...", section "Issue
+ * with parallel draft generation" (the target scores a whole draft tree in
+ * one pass and keeps the deepest root path it agrees with) and "Local LLM 4x
+ * Faster ..." (one verification pass over the tree).
  *   target_logits fp32 [T+1][V]: row 0 scores the children of the root (the
  *                  last committed token), row i+1 the children of node i
  *   draft_tokens  int32 [T]; parent int32 [T] with parent[i] < i, -1 = child

@@ -69,7 +69,7 @@ def _kind_of_param(decl: str) -> str:
 
 
 def _kind_of_ctype(t) -> str:
-    if t is ctypes.c_void_p or getattr(t, "_type_", None) is ctypes.c_void_p:
+    if t is ctypes.c_void_p or issubclass(t, ctypes._Pointer):
         return "pointer"
     if ctypes.sizeof(t) == 8:
         return "u64"
@@ -85,3 +85,28 @@ def test_binding_argument_lists_match_the_header():
         want = [_kind_of_param(p) for p in decl[name]]
         got = [_kind_of_ctype(t) for t in argtypes]
         assert got == want, (name, got, want)
+
+
+def _struct_fields(name):
+    """[(field type, field name)] of a typedef'd struct in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct " + name + r"\s*\{(.*?)\}", text, flags=re.S).group(1)
+    out = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        m = re.match(r"(.*?)(\w+(?:\s*,\s*\w+)*)$", decl)
+        ty, names = m.group(1).strip(), m.group(2)
+        for n in names.split(","):
+            out.append((ty, n.strip()))
+    return out
+
+
+def test_gemm_desc_layout_matches_the_header():
+    # the stack descriptor crosses the ABI as an array of structs: same fields,
+    # same order, same kinds
+    fields = _struct_fields("spec_gemm_desc")
+    assert [n for _, n in fields] == [n for n, _ in sv.GemmDesc._fields_]
+    for (ty, n), (_, ct) in zip(fields, sv.GemmDesc._fields_):
+        assert _kind_of_param(ty + (" *" if "*" in ty else "")) == _kind_of_ctype(ct), n

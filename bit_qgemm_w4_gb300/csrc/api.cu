@@ -378,7 +378,8 @@ int qgemm_stack_create(spec_ctx* ctx, const spec_gemm_desc* descs, int n, spec_g
       delete st;
       return rc;
     }
-    if (host[i].prep) st->any_prep = 1;
+    if (host[i].prep) st->prep_flags |= kAnyPrep;
+    if (host[i].xconv) st->prep_flags |= kAnyConv;
   }
   if (cudaMalloc(&st->dev_entries, sizeof(GemmEntry) * (size_t)n) != cudaSuccess) {
     delete st;

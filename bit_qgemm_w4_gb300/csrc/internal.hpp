@@ -18,6 +18,9 @@ constexpr int kGroupK = 64;                  // k per MMA group (one fp32 partia
 constexpr int kPartialSlotFloats = kMaxT * kTileM;
 constexpr int kMaxK = 32768;                 // rotated-activation buffer width
 constexpr int kSplitKeys = 4;                // GEMMs of one launch whose split tiles may overlap
+enum { kAnyPrep = 1, kAnyConv = 2 };         // a launch's prep_flags
+constexpr int kLocalConvStages = 32;         // GEMMs of at most this many stages per SM convert
+                                             // their activations in each CTA's shared memory
 constexpr int kGemmWorkers = 8;              // dequant/epilogue warps per CTA
 constexpr int kMaxStack = 1024;              // GEMMs per stack launch
 constexpr int kMaxAcceptT = 256;
@@ -79,7 +82,11 @@ struct alignas(64) GemmEntry {
   int y_f32;
   int wait_prev;
   int kind;                // operand form: kGemmBf16, kGemmF16Nib or kGemmF16
-  int prep;                // activations prepared inside the launch: 0 none, 1 rotated, 2 converted
+  int prep;                // activations prepared inside the launch by all CTAs into the
+                           // scratch copy: 0 none, 1 rotated, 2 converted to fp16
+  int xconv;               // activations converted to fp16 in each CTA's own shared-memory
+                           // slots as they arrive: 0 none, 1 fp16, 2 fp16 with the int4
+                           // column scaling
   uint32_t idesc;          // tcgen05.mma instruction descriptor (operand types, M, N)
 };
 
@@ -130,7 +137,7 @@ struct spec_gemm_stack {
   int quant = 0;
   int tpad = 0;
   int n = 0;
-  int any_prep = 0;
+  int prep_flags = 0;   // kAnyPrep | kAnyConv over the entries
   sv::GemmEntry* dev_entries = nullptr;   // [n] in device memory
 };
 

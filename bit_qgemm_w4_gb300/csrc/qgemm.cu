@@ -97,11 +97,14 @@ struct Cfg {
   static constexpr int kA0 = 128;
   static constexpr int kNAFit = (kTmemCols - kA0) / kACols;
   static constexpr int kNA = kNAFit > 4 ? 4 : kNAFit;
-  // warps: weight producer, activation producer, the TMEM owner, an idle
-  // warp (it keeps the MMA and worker warps on four-warp boundaries), the MMA
-  // warps, then the workers (any eight consecutive warps cover each TMEM lane
-  // quadrant twice)
+  // warps: weight producer, activation producer, the TMEM owner, a spare
+  // warp, the MMA warps, then the workers (any eight consecutive warps cover
+  // each TMEM lane quadrant twice).  Four warps, one per scheduler, convert
+  // activation slots in shared memory where a GEMM asks for it: the MMA
+  // warps, and with two MMA warps also warps 2 and 3.
   static constexpr int kWProd = 0, kXProd = 1, kAlloc = 2, kMma0 = 4;
+  static constexpr int kConvW = 4;
+  static constexpr int kConv0 = kMmaW == 4 ? kMma0 : 2;          // first converting warp
   static constexpr int kWorker0 = kMma0 + kMmaW;
   static constexpr int kThreads = 32 * (kWorker0 + kGemmWorkers);
   // one CTA per SM: the register file split evenly over its threads (a
@@ -115,14 +118,16 @@ struct Cfg {
   static_assert(kCols % 8 == 0, "epilogue columns in multiples of 8");
   static constexpr int kDM = 4;                                 // ring of per-stage "MMAs done" barriers
   static_assert(kNA <= kDM && kXSlots <= kDM, "a slot is reused within the done ring");
-  static_assert((2 * kWSlots + kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
+  static_assert((2 * kWSlots + 2 * kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
 };
 
 struct Params {
   const GemmEntry* entries;   // stack: device array; null: the entry passed by value
   int n_entries;
   int gate;                   // stack launch: count finished tiles, honour wait_prev
-  int any_prep;               // some entry prepares its activations (rotation counters in use)
+  int prep_flags;             // kAnyPrep: some entry prepares its activations with every CTA
+                              // (the rotation counters are in use); kAnyConv: some entry
+                              // converts its activation slots in shared memory
   int slot_ctas;              // CTAs per key in the split-tile slot arrays
   float* partials;            // [kSplitKeys][slot_ctas][128][TPAD] fp32, kept zeroed
   int* split_cnt;             // [kSplitKeys][slot_ctas][kGemmWorkers], kept zeroed
@@ -159,19 +164,18 @@ struct Ctl {
 };
 
 // Wait for a barrier phase; false on abort or when the limit passes.  A
-// phase that is not complete at the first probe is probed again after a
-// sleep that doubles up to `max_sleep_ns` (a probe returns at once here, and
-// a warp probing in a tight loop takes issue slots from the warps doing the
-// work); the abort flags and the clock are looked at on every eighth probe.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c,
-                                         uint32_t max_sleep_ns = 128) {
+// phase that is not complete at the first probe is waited for with the
+// suspending form of try_wait: the thread sleeps in hardware until the phase
+// completes or kSuspendNs passes, so it neither takes issue slots from the
+// warps doing the work nor oversleeps the flip; the abort flags and the clock
+// are looked at on every eighth probe.
+constexpr uint32_t kSuspendNs = 10000;
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  uint32_t ns = 16;
   for (uint32_t i = 1;; ++i) {
-    __nanosleep(ns);
-    if (ns < max_sleep_ns) ns <<= 1;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
     if ((i & 7u) == 0) {
       if (c.aborted()) return false;
       if (globaltimer() - t0 > c.limit) {
@@ -183,9 +187,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
 }
 
 // The same for a whole warp: every lane waits, and the outcome is uniform.
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Ctl& c,
-                                          uint32_t max_sleep_ns = 128) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, c, max_sleep_ns));
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Ctl& c) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, c));
 }
 
 // Wait until a device counter reaches `target` (acquire); false on abort or
@@ -500,6 +503,29 @@ __device__ __forceinline__ void finish_segment(const EpiEntry& en, const Walk& w
   }
 }
 
+// One converting warp's part of an activation slot (warp `cw` of kConvW):
+// wait until the slot has landed and, for a GEMM that converts in shared
+// memory, rewrite its share of the bf16 slot in place as the fp16 operand (a
+// 16-byte chunk holds 8 consecutive k at any swizzle position, so every
+// chunk stays where it is); then count the warp in on the slot's xconv
+// barrier.  False on abort or timeout.
+template <class C>
+__device__ __forceinline__ bool convert_slot(int mode, uint8_t* slot, uint64_t* full, uint64_t* conv,
+                                             uint32_t phase, int cw, int lane, const Ctl& ctl) {
+  if (!wait_warp(full, phase, ctl)) return false;
+  if (mode) {
+    constexpr int kChunks = C::kSub * C::kXBox / 16;
+    const bool nib = mode == 2;
+    uint4* c = reinterpret_cast<uint4*>(slot);
+#pragma unroll 4
+    for (int i = cw * 32 + lane; i < kChunks; i += C::kConvW * 32) c[i] = chunk_bf16_to_f16(c[i], nib);
+    fence_proxy_async_smem();   // the MMA reads the slot through the async proxy
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(conv);
+  return true;
+}
+
 template <int QUANT, int TPAD>
 __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     qgemm_kernel(const __grid_constant__ GemmEntry e0, const Params p) {
@@ -521,7 +547,10 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
   uint64_t* mdone = afull + NA;
   uint64_t* sfull = mdone + C::kDM;
   uint64_t* sempty = sfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
+  // xconv[s]: the activation slot holds the MMA's operand form (after the
+  // converters, for GEMMs that convert in shared memory)
+  uint64_t* xconv = sempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xconv + SX);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const GemmEntry* E = p.entries ? p.entries : &e0;
@@ -536,7 +565,10 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], kGemmWorkers);
     }
-    for (int s = 0; s < SX; ++s) mbar_init(&xfull[s], 1);
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xconv[s], C::kConvW);
+    }
     for (int s = 0; s < NA; ++s) mbar_init(&afull[s], kGemmWorkers);
     for (int s = 0; s < C::kDM; ++s) mbar_init(&mdone[s], C::kMmaW);   // one commit per MMA warp
     for (int s = 0; s < 2; ++s) {
@@ -612,7 +644,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         while (pf.valid() && pf_n < n + p.pf_max &&
                !__all_sync(0xffffffffu, mbar_test_wait(&wempty[r.slot], r.phase ^ 1)))
           prefetch_next();
-        if (!wait_warp(&wempty[r.slot], r.phase ^ 1, ctl, 512)) break;
+        if (!wait_warp(&wempty[r.slot], r.phase ^ 1, ctl)) break;
       }
       if (n == p.skip_unit && cta == 0) {
         skipped = n;   // test hook: this stage's weights never arrive
@@ -715,7 +747,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       int kst = ub % ks;
       for (int u = ub; u < ue; ++u, r.next(), ++n) {
         if (n >= SX) {
-          if (!wait_warp(&mdone[rdone.slot], rdone.phase, ctl, 512)) {
+          if (!wait_warp(&mdone[rdone.slot], rdone.phase, ctl)) {
             ok = false;
             break;
           }
@@ -736,7 +768,17 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       for (int j = (n > SX ? n - SX : 0); j < n; ++j) drain_bar(&xfull[j % SX], (uint32_t)((j / SX) & 1));
     }
   } else if (warp < C::kMma0) {
-    // the TMEM owner and the idle warp wait at the final barrier
+    // ------------------------------------------------------------ converters
+    // (warps 2 and 3 when there are two MMA warps; else they wait at the
+    // final barrier)
+    if (C::kConv0 == 2 && (p.prep_flags & kAnyConv)) {
+      Walk w(E, nE, G, cta);
+      Ring<SX> r;
+      for (; w.valid(); w.next(), r.next())
+        if (!convert_slot<C>(E[w.e].xconv, xreg + r.slot * C::kXSlot, &xfull[r.slot], &xconv[r.slot],
+                             r.phase, warp - C::kConv0, lane, ctl))
+          break;
+    }
   } else if (warp < C::kWorker0) {
     // ------------------------------------------------------------ MMA issue
     // warp kMma0 + k issues the K16 MMAs of groups k*kGpm .. into its own
@@ -750,20 +792,26 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     Ring<SX> rx;
     Ring<C::kDM> rm;
     Ring<2> rs;
-    int ce = -1, last_m = -1;
+    int ce = -1, last_m = -1, xconv_mode = 0;
+    const bool any_conv = (p.prep_flags & kAnyConv) != 0;
     uint32_t idesc = 0, last_mph = 0;
     for (; w.valid(); w.next(), ra.next(), rx.next(), rm.next()) {
       if (w.e != ce) {
         ce = w.e;
         idesc = E[ce].idesc;
+        xconv_mode = E[ce].xconv;
       }
       const bool seg0 = w.kst == 0 || w.u == w.ub;
       const bool seg1 = w.kst == w.ks - 1 || w.u == w.ue - 1;
+      if (any_conv && !convert_slot<C>(xconv_mode, xreg + rx.slot * C::kXSlot, &xfull[rx.slot], &xconv[rx.slot],
+                                       rx.phase, warp - C::kConv0, lane, ctl))
+        break;
       // a segment starts on a zeroed accumulator (zeroed at the start of the
       // launch, then by the workers after they read it)
       if (seg0 && !wait_warp(&sempty[rs.slot], rs.phase, ctl)) break;
       if (!wait_warp(&afull[ra.slot], ra.phase, ctl)) break;
-      if (!wait_warp(&xfull[rx.slot], rx.phase, ctl)) break;
+      // a converted slot is ready once every converting warp has done its share
+      if (!wait_warp(xconv_mode ? &xconv[rx.slot] : &xfull[rx.slot], rx.phase, ctl)) break;
       tc_fence_after();
       if (leader) {
         const uint32_t d = tbase + rs.slot * C::kDCols;
@@ -957,7 +1005,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
-  if (threadIdx.x == 0 && (p.gate || p.any_prep)) {
+  if (threadIdx.x == 0 && (p.gate || (p.prep_flags & kAnyPrep))) {
     // the last CTA to leave resets the per-entry counters for the next launch
     __threadfence();
     const int old = atomic_add_acq_rel_gpu(p.exit_cnt, 1);
@@ -974,13 +1022,13 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
 
 template <int QUANT, int TPAD>
 int launch_t(spec_ctx* ctx, const GemmEntry& e0, const GemmEntry* dev_entries, int n, int gate,
-             int any_prep, int G, cudaStream_t stream) {
+             int prep_flags, int G, cudaStream_t stream) {
   using C = Cfg<QUANT, TPAD>;
   Params p;
   p.entries = dev_entries;
   p.n_entries = n;
   p.gate = gate;
-  p.any_prep = any_prep;
+  p.prep_flags = prep_flags;
   p.slot_ctas = ctx->num_sms;
   p.partials = ctx->partials;
   p.split_cnt = ctx->split_cnt;
@@ -1022,12 +1070,12 @@ int launch_t(spec_ctx* ctx, const GemmEntry& e0, const GemmEntry* dev_entries, i
 
 template <int QUANT>
 int launch_q(spec_ctx* ctx, int tpad, const GemmEntry& e0, const GemmEntry* dev, int n, int gate,
-             int any_prep, int G, cudaStream_t s) {
+             int prep_flags, int G, cudaStream_t s) {
   switch (tpad) {
-    case 16: return launch_t<QUANT, 16>(ctx, e0, dev, n, gate, any_prep, G, s);
-    case 32: return launch_t<QUANT, 32>(ctx, e0, dev, n, gate, any_prep, G, s);
-    case 48: return launch_t<QUANT, 48>(ctx, e0, dev, n, gate, any_prep, G, s);
-    case 64: return launch_t<QUANT, 64>(ctx, e0, dev, n, gate, any_prep, G, s);
+    case 16: return launch_t<QUANT, 16>(ctx, e0, dev, n, gate, prep_flags, G, s);
+    case 32: return launch_t<QUANT, 32>(ctx, e0, dev, n, gate, prep_flags, G, s);
+    case 48: return launch_t<QUANT, 48>(ctx, e0, dev, n, gate, prep_flags, G, s);
+    case 64: return launch_t<QUANT, 64>(ctx, e0, dev, n, gate, prep_flags, G, s);
     default: return set_error(SPEC_ERR_SHAPE, "padded T=%d outside 16..64", tpad);
   }
 }
@@ -1050,7 +1098,14 @@ int build_entry(spec_ctx* ctx, const GemmArgs& a, int tpad, int index, GemmEntry
   // activations the MMA reads in another form are prepared inside the launch
   // into the scratch copy of this GEMM's key (a rotated bf16 GEMM's as 2T
   // rows, (rounded, remainder) per token)
-  const int prep = rot ? 1 : (kind != kGemmBf16 ? 2 : 0);
+  // small GEMMs convert each CTA's activation slots in shared memory; large
+  // ones (many stages per CTA, each slot read many times) convert once, with
+  // every CTA taking a share, into the scratch copy
+  const long long units = (long long)((a.K + SK - 1) / SK) * ((a.N + kTileM - 1) / kTileM);
+  const int xconv = !rot && kind != kGemmBf16 && units <= (long long)kLocalConvStages * ctx->num_sms
+                        ? (kind == kGemmF16Nib ? 2 : 1)
+                        : 0;
+  const int prep = rot ? 1 : (kind != kGemmBf16 && !xconv ? 2 : 0);
   uint16_t* xp = prep ? ctx->xprep + (size_t)(index % kSplitKeys) * kMaxT * kMaxK : nullptr;
   const uint16_t* xsrc = prep ? xp : a.x;
   const uint64_t xrows = rot && kind == kGemmBf16 ? 2 * (uint64_t)a.T : (uint64_t)a.T;
@@ -1097,6 +1152,7 @@ int build_entry(spec_ctx* ctx, const GemmArgs& a, int tpad, int index, GemmEntry
   e.wait_prev = a.wait_prev;
   e.kind = kind;
   e.prep = prep;
+  e.xconv = xconv;
   e.idesc = kind == kGemmBf16 ? idesc_bf16_f32(128, tpad) : idesc_f16_f32(128, tpad);
   *out = e;
   return SPEC_OK;
@@ -1118,16 +1174,17 @@ int launch_qgemm(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const long long per = (e.units + G - 1) / G;
   G = (e.units + per - 1) / per;
   if (e.prep) G = ctx->num_sms < e.units ? ctx->num_sms : e.units;
-  return a.quant == kW4 ? launch_q<kW4>(ctx, tpad, e, nullptr, 1, 0, e.prep != 0, (int)G, s)
-                        : launch_q<kW8>(ctx, tpad, e, nullptr, 1, 0, e.prep != 0, (int)G, s);
+  const int flags = (e.prep ? kAnyPrep : 0) | (e.xconv ? kAnyConv : 0);
+  return a.quant == kW4 ? launch_q<kW4>(ctx, tpad, e, nullptr, 1, 0, flags, (int)G, s)
+                        : launch_q<kW8>(ctx, tpad, e, nullptr, 1, 0, flags, (int)G, s);
 }
 
 int launch_qgemm_stack(spec_ctx* ctx, const spec_gemm_stack* st, cudaStream_t s) {
   GemmEntry dummy;
   std::memset(&dummy, 0, sizeof(dummy));
   return st->quant == kW4
-             ? launch_q<kW4>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->any_prep, ctx->num_sms, s)
-             : launch_q<kW8>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->any_prep, ctx->num_sms, s);
+             ? launch_q<kW4>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->prep_flags, ctx->num_sms, s)
+             : launch_q<kW8>(ctx, st->tpad, dummy, st->dev_entries, st->n, 1, st->prep_flags, ctx->num_sms, s);
 }
 
 }  // namespace sv

@@ -64,6 +64,11 @@ namespace {
 
 constexpr int kTmemCols = 512;
 
+// flags of a stage's control record (bits above the GEMM index)
+constexpr uint32_t kStageSegEnd = 1u << 16;   // the CTA's segment of the tile ends here
+constexpr uint32_t kStageWhole = 1u << 17;    // ... and it covered the whole tile
+constexpr uint32_t kStageLast = 1u << 18;     // the CTA's last stage of the launch
+
 template <int QUANT, int TPAD>
 struct Cfg {
   static constexpr int kSub = QUANT == kW4 ? 4 : 2;             // 64-k groups per stage
@@ -79,6 +84,10 @@ struct Cfg {
   static constexpr int kScaleOff = kTileM * 128;
   static constexpr int kZeroOff = kScaleOff + kSub * kTileM * 2;
   static constexpr int kWSlot = (kZeroOff + (QUANT == kW4 ? kSub * 64 : 0) + 1023) / 1024 * 1024;
+  // the stage's control record (written by the weight producer): the GEMM
+  // index with the kStage* flags, then the tile
+  static constexpr int kCtlOff = kWSlot - 16;
+  static_assert(kCtlOff >= kZeroOff + (QUANT == kW4 ? kSub * 64 : 0), "control record inside the slot padding");
   // activation slot: kSub boxes [TPAD][64] 16-bit (128-byte rows, 128-byte swizzle)
   static constexpr int kXBox = TPAD * 128;
   static constexpr int kXSlot = kSub * kXBox;
@@ -260,7 +269,7 @@ struct Ring {
 struct Walk {
   const GemmEntry* E;
   int nE, G, c;
-  int e, u, ub, ue, tile, kst, ks;
+  int e = 0, u = 0, ub = 0, ue = 0, tile = 0, kst = 0, ks = 1;
   __device__ __forceinline__ Walk(const GemmEntry* E_, int nE_, int G_, int c_)
       : E(E_), nE(nE_), G(G_), c(c_) {
     enter(0);
@@ -292,28 +301,13 @@ struct Walk {
   }
 };
 
-// Counts a CTA's units across the entries (entry index only), for roles
-// that need no tile coordinates.
-struct Count {
-  const GemmEntry* E;
-  int nE, G, c;
-  int e, rem;
-  __device__ __forceinline__ Count(const GemmEntry* E_, int nE_, int G_, int c_)
-      : E(E_), nE(nE_), G(G_), c(c_) {
-    enter(0);
-  }
-  __device__ __forceinline__ void enter(int e0) {
-    for (e = e0; e < nE; ++e) {
-      const int U = E[e].units;
-      rem = unit_begin(c + 1, U, G) - unit_begin(c, U, G);
-      if (rem > 0) return;
-    }
-  }
-  __device__ __forceinline__ bool valid() const { return e < nE; }
-  __device__ __forceinline__ void next() {
-    if (--rem == 0) enter(e + 1);
-  }
-};
+// The last GEMM of the launch in which CTA c owns a stage, or -1.
+__device__ __forceinline__ int last_entry_of(const GemmEntry* E, int nE, int G, int c) {
+  int e = nE - 1;
+  while (e >= 0 && unit_begin(c + 1, E[e].units, G) <= unit_begin(c, E[e].units, G)) --e;
+  return e;
+}
+
 
 // int4: the 64 codes of group j of a row's 128-byte stage line.  The line was
 // written by TMA with the 128-byte swizzle: 16-byte chunk c of row m sits at
@@ -425,13 +419,11 @@ struct EpiEntry {
 // a split tile is summed into its fp32 slot and finished by the last
 // contributor to arrive.
 template <int QUANT, int TPAD>
-__device__ __forceinline__ void finish_segment(const EpiEntry& en, const Walk& we, bool seg_from0,
+__device__ __forceinline__ void finish_segment(const EpiEntry& en, int tile, bool whole,
                                             float (&v)[Cfg<QUANT, TPAD>::kCols], const Params& p,
                                             int m, int c0, int wk, int lane) {
   constexpr int kCols = Cfg<QUANT, TPAD>::kCols;
-  const int tile = we.tile;
   const int row = tile * kTileM + m;
-  const bool whole = seg_from0 && we.kst == we.ks - 1;
   if (en.per_channel) {
     const float osc = row < en.N ? __half2float(__ushort_as_half(en.chscale[row])) : 1.f;
 #pragma unroll
@@ -604,9 +596,9 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     // a GEMM's tensor maps and stage sizes, cached while the walk stays in it
     struct Src {
       int e = -1;
-      const CUtensorMap *codes, *scales, *zeros;
-      uint32_t tx;
-      int rows, gshift;
+      const CUtensorMap *codes = nullptr, *scales = nullptr, *zeros = nullptr;
+      uint32_t tx = 0;
+      int rows = 0, gshift = 0;
       __device__ __forceinline__ void at(const GemmEntry* E, int e_) {
         if (e_ == e) return;
         e = e_;
@@ -624,6 +616,8 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     int pf_n = 0;
     Ring<SW> r;
     int n = 0, skipped = -1;
+    const int last_e = last_entry_of(E, nE, G, cta);
+    bool from0 = false;
     auto prefetch_next = [&]() {
       spf.at(E, pf.e);
       if (leader) {
@@ -651,8 +645,14 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         continue;
       }
       sw.at(E, w.e);
+      if (w.kst == 0 || w.u == w.ub) from0 = w.kst == 0;
+      const bool seg_end = w.kst == w.ks - 1 || w.u == w.ue - 1;
+      const uint32_t rec = (uint32_t)w.e | (seg_end ? kStageSegEnd : 0u) |
+                           (seg_end && from0 && w.kst == w.ks - 1 ? kStageWhole : 0u) |
+                           (w.e == last_e && w.u == w.ue - 1 ? kStageLast : 0u);
       if (leader) {
         uint8_t* st = wreg + r.slot * C::kWSlot;
+        *reinterpret_cast<uint2*>(st + C::kCtlOff) = make_uint2(rec, (uint32_t)w.tile);
         mbar_arrive_expect_tx(&wfull[r.slot], sw.tx);
         tma_load_2d_hint(st, sw.codes, &wfull[r.slot], w.kst * 128, w.tile * kTileM, pol);
         if (sw.rows) {
@@ -848,11 +848,9 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t zshift = (m & 1) * 4;
     const uint32_t wbase = smem_u32(wreg);
-    Count wd(E, nE, G, cta);                      // stage being dequantised (n)
-    Walk we(E, nE, G, cta);                       // stage whose segment may end (n - 1)
     // per-entry shared-memory offsets inside a weight slot: this row's zero
     // byte and scale of each dequantised group
-    uint32_t zoff[C::kGpw], soff[C::kGpw];
+    uint32_t zoff[C::kGpw] = {}, soff[C::kGpw] = {};
     int ed = -1, ee = -1, kind = 0;
     EpiEntry epi{};
     auto enter_d = [&](int e) {
@@ -890,9 +888,16 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     };
     Ring<SW> rw;
     Ring<NA> ra;
-    Ring<C::kDM> rm;        // stage whose MMAs free the A slot: n - NA
+    // stage n reuses the A slot of stage n - NA once that stage's MMAs are
+    // done: ring position n - NA + kDM, so the first NA waits name the phase
+    // before a barrier's first one, which counts as complete
+    Ring<C::kDM> rm;
+    rm.slot = C::kDM - NA;
+    rm.phase = 1;
     Ring<2> rs;
-    bool seg_from0 = false, ok = true;
+    bool ok = true, pdl_done = false;
+    bool more = last_entry_of(E, nE, G, cta) >= 0;   // this CTA owns any stage
+    uint32_t prec = 0, ptile = 0;                     // the previous stage's control record
     // both accumulators start at zero
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl) tmem_zero_cols<kCols>(tbase + lane_base + sl * C::kDCols + c0);
@@ -903,18 +908,22 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       mbar_arrive(&sempty[0]);
       mbar_arrive(&sempty[1]);
     }
-    for (int n = 0;; ++n) {
-      const bool has_d = wd.valid();
-      const bool has_e = n > 0 && we.valid();
-      if (!has_d && !has_e) break;
+    for (;;) {
+      const bool has_d = more;
+      uint32_t rec = 0, tile = 0;
       if (has_d) {
-        // ---- dequantise stage n into A slot n % NA
-        if (wd.e != ed) enter_d(wd.e);
+        // ---- dequantise the next stage into its A slot
         if (!wait_warp(&wfull[rw.slot], rw.phase, ctl)) {
           ok = false;
           break;
         }
         const uint32_t st = wbase + rw.slot * C::kWSlot;
+        {
+          const uint2 r2 = lds64(st + C::kCtlOff);
+          rec = r2.x;
+          tile = r2.y;
+        }
+        if ((int)(rec & 0xFFFFu) != ed) enter_d((int)(rec & 0xFFFFu));
         uint32_t words[C::kGpw][8];
         uint32_t zb[C::kGpw], s2[C::kGpw];
         if constexpr (QUANT == kW4) {
@@ -928,14 +937,12 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
 #pragma unroll
           for (int i = 0; i < C::kGpw; ++i) s2[i] = kind == kGemmF16 ? (uint32_t)lds_u16(st + soff[i]) * 0x00010001u : 0u;
         }
-        // the A slot is free once the MMAs that read it (stage n - NA) have completed
-        if (n >= NA) {
-          if (!wait_warp(&mdone[rm.slot], rm.phase, ctl)) {
-            ok = false;
-            break;
-          }
-          rm.next();
+        // the A slot is free once the MMAs that read it (NA stages back) have completed
+        if (!wait_warp(&mdone[rm.slot], rm.phase, ctl)) {
+          ok = false;
+          break;
         }
+        rm.next();
         tc_fence_after();
         const uint32_t aslot = tbase + lane_base + C::kA0 + ra.slot * C::kACols;
 #pragma unroll
@@ -958,40 +965,39 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
           mbar_arrive(&afull[ra.slot]);
           mbar_arrive(&wempty[rw.slot]);   // codes, scales and zero points read
         }
-      }
-      if (has_e) {
-        // ---- stage n - 1: the end of a segment reads the accumulators
-        if (n == 1) {
-          // outputs and split-tile sums may still be used by the previous kernel
-          pdl_wait_prior();
-        }
-        if (we.kst == 0 || we.u == we.ub) seg_from0 = we.kst == 0;
-        if (we.kst == we.ks - 1 || we.u == we.ue - 1) {
-          if (we.e != ee) enter_e(we.e);
-          if (!wait_warp(&sfull[rs.slot], rs.phase, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t dbase = tbase + lane_base + rs.slot * C::kDCols + c0;
-          float v[kCols];
-          tmem_ld_cols<kCols>(dbase, v);
-          tmem_wait_ld();
-          tmem_zero_cols<kCols>(dbase);     // the next segment on this accumulator adds from zero
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sempty[rs.slot]);
-          rs.next();
-          finish_segment<QUANT, TPAD>(epi, we, seg_from0, v, p, m, c0, wk, lane);
-        }
-        we.next();
-      }
-      if (has_d) {
-        wd.next();
         rw.next();
         ra.next();
+        if (rec & kStageLast) more = false;
       }
+      // ---- the previous stage: the end of a segment reads the accumulator
+      // (one stage late, so that its MMAs complete behind this dequantisation)
+      if (prec & kStageSegEnd) {
+        if (!pdl_done) {
+          // outputs and split-tile sums may still be used by the previous kernel
+          pdl_wait_prior();
+          pdl_done = true;
+        }
+        if ((int)(prec & 0xFFFFu) != ee) enter_e((int)(prec & 0xFFFFu));
+        if (!wait_warp(&sfull[rs.slot], rs.phase, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dbase = tbase + lane_base + rs.slot * C::kDCols + c0;
+        float v[kCols];
+        tmem_ld_cols<kCols>(dbase, v);
+        tmem_wait_ld();
+        tmem_zero_cols<kCols>(dbase);     // the next segment on this accumulator adds from zero
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[rs.slot]);
+        rs.next();
+        finish_segment<QUANT, TPAD>(epi, (int)ptile, (prec & kStageWhole) != 0, v, p, m, c0, wk, lane);
+      }
+      if (!has_d) break;
+      prec = rec;
+      ptile = tile;
     }
     if (!ok) {
       tmem_wait_st();

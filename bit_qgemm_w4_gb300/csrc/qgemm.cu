@@ -127,7 +127,7 @@ struct Cfg {
   static_assert(kCols % 8 == 0, "epilogue columns in multiples of 8");
   static constexpr int kDM = 4;                                 // ring of per-stage "MMAs done" barriers
   static_assert(kNA <= kDM && kXSlots <= kDM, "a slot is reused within the done ring");
-  static_assert((2 * kWSlots + 2 * kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
+  static_assert((2 * kWSlots + 3 * kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
 };
 
 struct Params {
@@ -495,16 +495,13 @@ __device__ __forceinline__ void finish_segment(const EpiEntry& en, int tile, boo
   }
 }
 
-// One converting warp's part of an activation slot (warp `cw` of kConvW):
-// wait until the slot has landed and, for a GEMM that converts in shared
-// memory, rewrite its share of the bf16 slot in place as the fp16 operand (a
-// 16-byte chunk holds 8 consecutive k at any swizzle position, so every
-// chunk stays where it is); then count the warp in on the slot's xconv
-// barrier.  False on abort or timeout.
+// One converting warp's part of a landed activation slot (warp `cw` of
+// kConvW): for a GEMM that converts in shared memory, rewrite its share of
+// the bf16 slot in place as the fp16 operand (a 16-byte chunk holds 8
+// consecutive k at any swizzle position, so every chunk stays where it is);
+// then count the warp in on the slot's xconv barrier.
 template <class C>
-__device__ __forceinline__ bool convert_slot(int mode, uint8_t* slot, uint64_t* full, uint64_t* conv,
-                                             uint32_t phase, int cw, int lane, const Ctl& ctl) {
-  if (!wait_warp(full, phase, ctl)) return false;
+__device__ __forceinline__ void convert_share(int mode, uint8_t* slot, uint64_t* conv, int cw, int lane) {
   if (mode) {
     constexpr int kChunks = C::kSub * C::kXBox / 16;
     const bool nib = mode == 2;
@@ -515,7 +512,6 @@ __device__ __forceinline__ bool convert_slot(int mode, uint8_t* slot, uint64_t* 
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(conv);
-  return true;
 }
 
 template <int QUANT, int TPAD>
@@ -542,7 +538,10 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
   // xconv[s]: the activation slot holds the MMA's operand form (after the
   // converters, for GEMMs that convert in shared memory)
   uint64_t* xconv = sempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xconv + SX);
+  // xrec[s]: the control record of the stage in activation slot s (written
+  // by the activation producer before the slot's copies)
+  uint2* xrec = reinterpret_cast<uint2*>(xconv + SX);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xrec + SX);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const GemmEntry* E = p.entries ? p.entries : &e0;
@@ -678,6 +677,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     Ring<C::kDM> rdone;     // stage whose MMAs free the slot: n - SX
     int n = 0, verified = 0;
     bool ok = true;
+    const int last_e = last_entry_of(E, nE, G, cta);
     for (int e = 0; e < nE && ok; ++e) {
       const GemmEntry& en = E[e];
       const int ub = unit_begin(cta, en.units, G), ue = unit_begin(cta + 1, en.units, G);
@@ -755,6 +755,10 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         }
         if (leader) {
           uint8_t* st = xreg + r.slot * C::kXSlot;
+          const bool seg_end = kst == ks - 1 || u == ue - 1;
+          xrec[r.slot] = make_uint2((uint32_t)e | (seg_end ? kStageSegEnd : 0u) |
+                                        (e == last_e && u == ue - 1 ? kStageLast : 0u),
+                                    0u);
           mbar_arrive_expect_tx(&xfull[r.slot], (uint32_t)(SUB * C::kXBox));
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
@@ -772,21 +776,26 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     // (warps 2 and 3 when there are two MMA warps; else they wait at the
     // final barrier)
     if (C::kConv0 == 2 && (p.prep_flags & kAnyConv)) {
-      Walk w(E, nE, G, cta);
       Ring<SX> r;
-      for (; w.valid(); w.next(), r.next())
-        if (!convert_slot<C>(E[w.e].xconv, xreg + r.slot * C::kXSlot, &xfull[r.slot], &xconv[r.slot],
-                             r.phase, warp - C::kConv0, lane, ctl))
-          break;
+      int ce = -1, mode = 0;
+      for (bool more = last_entry_of(E, nE, G, cta) >= 0; more; r.next()) {
+        if (!wait_warp(&xfull[r.slot], r.phase, ctl)) break;
+        const uint32_t rec = xrec[r.slot].x;
+        if ((int)(rec & 0xFFFFu) != ce) {
+          ce = (int)(rec & 0xFFFFu);
+          mode = E[ce].xconv;
+        }
+        convert_share<C>(mode, xreg + r.slot * C::kXSlot, &xconv[r.slot], warp - C::kConv0, lane);
+        if (rec & kStageLast) more = false;
+      }
     }
   } else if (warp < C::kWorker0) {
     // ------------------------------------------------------------ MMA issue
-    // warp kMma0 + k issues the K16 MMAs of groups k*kGpm .. into its own
-    // accumulator of the current segment's set (the whole warp walks; one
-    // elected lane issues)
+    // warp kMma0 + k issues the K16 MMAs of groups k*kGpm .. into the
+    // current segment's accumulator (the whole warp follows the activation
+    // slots' control records; one elected lane issues)
     const int k = warp - C::kMma0;
     const bool leader = elect_one();
-    Walk w(E, nE, G, cta);
     const uint64_t xdesc0 = smem_desc_sw128(xreg);
     Ring<NA> ra;
     Ring<SX> rx;
@@ -795,24 +804,25 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     int ce = -1, last_m = -1, xconv_mode = 0;
     const bool any_conv = (p.prep_flags & kAnyConv) != 0;
     uint32_t idesc = 0, last_mph = 0;
-    for (; w.valid(); w.next(), ra.next(), rx.next(), rm.next()) {
-      if (w.e != ce) {
-        ce = w.e;
+    bool seg_start = true;
+    for (bool more = last_entry_of(E, nE, G, cta) >= 0; more;) {
+      // the stage's activations (and its control record) have landed
+      if (!wait_warp(&xfull[rx.slot], rx.phase, ctl)) break;
+      const uint32_t rec = xrec[rx.slot].x;
+      if ((int)(rec & 0xFFFFu) != ce) {
+        ce = (int)(rec & 0xFFFFu);
         idesc = E[ce].idesc;
         xconv_mode = E[ce].xconv;
       }
-      const bool seg0 = w.kst == 0 || w.u == w.ub;
-      const bool seg1 = w.kst == w.ks - 1 || w.u == w.ue - 1;
-      if (any_conv && !convert_slot<C>(xconv_mode, xreg + rx.slot * C::kXSlot, &xfull[rx.slot], &xconv[rx.slot],
-                                       rx.phase, warp - C::kConv0, lane, ctl))
-        break;
+      if (any_conv) convert_share<C>(xconv_mode, xreg + rx.slot * C::kXSlot, &xconv[rx.slot], warp - C::kConv0, lane);
       // a segment starts on a zeroed accumulator (zeroed at the start of the
       // launch, then by the workers after they read it)
-      if (seg0 && !wait_warp(&sempty[rs.slot], rs.phase, ctl)) break;
+      if (seg_start && !wait_warp(&sempty[rs.slot], rs.phase, ctl)) break;
       if (!wait_warp(&afull[ra.slot], ra.phase, ctl)) break;
       // a converted slot is ready once every converting warp has done its share
-      if (!wait_warp(xconv_mode ? &xconv[rx.slot] : &xfull[rx.slot], rx.phase, ctl)) break;
+      if (xconv_mode && !wait_warp(&xconv[rx.slot], rx.phase, ctl)) break;
       tc_fence_after();
+      const bool seg_end = (rec & kStageSegEnd) != 0;
       if (leader) {
         const uint32_t d = tbase + rs.slot * C::kDCols;
         const uint32_t a0 = tbase + C::kA0 + ra.slot * C::kACols;
@@ -827,12 +837,17 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
           }
         }
         mma_commit(&mdone[rm.slot]);
-        if (seg1) mma_commit(&sfull[rs.slot]);
+        if (seg_end) mma_commit(&sfull[rs.slot]);
       }
       __syncwarp();
       last_m = rm.slot;
       last_mph = rm.phase;
-      if (seg1) rs.next();
+      if (seg_end) rs.next();
+      seg_start = seg_end;
+      ra.next();
+      rx.next();
+      rm.next();
+      if (rec & kStageLast) more = false;
     }
     // the CTA frees its tensor memory and shared memory only after its
     // MMAs have completed and their commits have arrived

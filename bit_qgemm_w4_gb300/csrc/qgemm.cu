@@ -68,6 +68,8 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kStageSegEnd = 1u << 16;   // the CTA's segment of the tile ends here
 constexpr uint32_t kStageWhole = 1u << 17;    // ... and it covered the whole tile
 constexpr uint32_t kStageLast = 1u << 18;     // the CTA's last stage of the launch
+constexpr uint32_t kStageFrom0 = 1u << 19;    // (at a segment end) the segment began at the tile's first k
+constexpr uint32_t kStageFinStart = 1u << 20; // first stage of a segment that finishes a split tile
 
 template <int QUANT, int TPAD>
 struct Cfg {
@@ -415,13 +417,20 @@ struct EpiEntry {
 };
 
 // End of a worker's segment of a tile: v holds its rows m, accumulator
-// columns c0.. of the CTA's share of the tile.  A whole tile is written out;
-// a split tile is summed into its fp32 slot and finished by the last
-// contributor to arrive.
+// columns c0.. of the CTA's share of the tile.  A whole tile is written out.
+// A tile split over several CTAs is finished by its first contributor (the
+// CTA holding its first k, whose share is the last segment of its range and
+// so, in time, usually the last to complete): every other contributor adds
+// its part into the tile's fp32 slot and counts itself in with a release;
+// the finisher adds the slot's sum (fetched early into `pre` when the
+// others had already counted in, else waited for here) to its own part.
+// False when that wait gives up (abort or time limit).
 template <int QUANT, int TPAD>
-__device__ __forceinline__ void finish_segment(const EpiEntry& en, int tile, bool whole,
-                                            float (&v)[Cfg<QUANT, TPAD>::kCols], const Params& p,
-                                            int m, int c0, int wk, int lane) {
+__device__ __forceinline__ bool finish_segment(const EpiEntry& en, int tile, bool whole, bool from0,
+                                            float (&v)[Cfg<QUANT, TPAD>::kCols],
+                                            float (&pre)[Cfg<QUANT, TPAD>::kCols], bool& pre_ok,
+                                            const Params& p, int m, int c0, int wk, int lane,
+                                            const Ctl& ctl) {
   constexpr int kCols = Cfg<QUANT, TPAD>::kCols;
   const int row = tile * kTileM + m;
   if (en.per_channel) {
@@ -431,31 +440,38 @@ __device__ __forceinline__ void finish_segment(const EpiEntry& en, int tile, boo
   }
   bool finished = whole;
   if (!whole) {
-    // split tile: add this warp's part into the tile's fp32 slot (keyed by
-    // the entry and the tile's first contributor, unique among the split
-    // tiles in flight); the last contributor to arrive finishes it
+    // the tile's fp32 slot and counters are keyed by the entry and the
+    // tile's first contributor (unique among the split tiles in flight)
     const bool a = tile == en.tile_a;
     const int c_first = a ? en.first_a : en.first_b;
     const int c_last = a ? en.last_a : en.last_b;
     const size_t key = (size_t)(en.e % kSplitKeys) * p.slot_ctas + c_first;
     float* slot = p.partials + (key * kTileM + m) * TPAD + c0;
-#pragma unroll
-    for (int c = 0; c < kCols; c += 4) red_add_f32x4(slot + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
-    __syncwarp();
     int* cnt = p.split_cnt + key * kGemmWorkers + wk;
-    int last = 0;
-    if (lane == 0) last = atomic_add_acq_rel_gpu(cnt, 1) == c_last - c_first;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    __syncwarp();   // orders lane 0's acquire before the other lanes' reads
-    if (last) {
+    if (!from0) {
 #pragma unroll
-      for (int c = 0; c < kCols; c += 4) {
-        const float4 s4 = ldcg_f32x4(slot + c);
-        v[c] = s4.x;
-        v[c + 1] = s4.y;
-        v[c + 2] = s4.z;
-        v[c + 3] = s4.w;
+      for (int c = 0; c < kCols; c += 4) red_add_f32x4(slot + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(cnt, 1);
+    } else {
+      if (!pre_ok) {
+        int ready = 1;
+        if (lane == 0) ready = wait_count(cnt, c_last - c_first, ctl) ? 1 : 0;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        __syncwarp();   // orders lane 0's acquire before the other lanes' reads
+        if (!ready) return false;
+#pragma unroll
+        for (int c = 0; c < kCols; c += 4) {
+          const float4 s4 = ldcg_f32x4(slot + c);
+          pre[c] = s4.x;
+          pre[c + 1] = s4.y;
+          pre[c + 2] = s4.z;
+          pre[c + 3] = s4.w;
+        }
       }
+      pre_ok = false;
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) v[c] += pre[c];
 #pragma unroll
       for (int c = 0; c < kCols; c += 4)
         __stcg(reinterpret_cast<float4*>(slot + c), make_float4(0.f, 0.f, 0.f, 0.f));
@@ -493,6 +509,7 @@ __device__ __forceinline__ void finish_segment(const EpiEntry& en, int tile, boo
       if (lane == 0) red_release_gpu_add(&p.done[en.e], 1);
     }
   }
+  return true;
 }
 
 // One converting warp's part of a landed activation slot (warp `cw` of
@@ -644,10 +661,15 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         continue;
       }
       sw.at(E, w.e);
-      if (w.kst == 0 || w.u == w.ub) from0 = w.kst == 0;
+      const bool seg_start = w.kst == 0 || w.u == w.ub;
+      if (seg_start) from0 = w.kst == 0;
       const bool seg_end = w.kst == w.ks - 1 || w.u == w.ue - 1;
+      // a segment from the tile's first k that stops before its last one
+      // finishes a tile split over several CTAs
+      const bool fin_start = seg_start && w.kst == 0 && w.u - w.kst + w.ks > w.ue;
       const uint32_t rec = (uint32_t)w.e | (seg_end ? kStageSegEnd : 0u) |
                            (seg_end && from0 && w.kst == w.ks - 1 ? kStageWhole : 0u) |
+                           (seg_end && from0 ? kStageFrom0 : 0u) | (fin_start ? kStageFinStart : 0u) |
                            (w.e == last_e && w.u == w.ue - 1 ? kStageLast : 0u);
       if (leader) {
         uint8_t* st = wreg + r.slot * C::kWSlot;
@@ -913,6 +935,11 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     bool ok = true, pdl_done = false;
     bool more = last_entry_of(E, nE, G, cta) >= 0;   // this CTA owns any stage
     uint32_t prec = 0, ptile = 0;                     // the previous stage's control record
+    // the other contributors' sum of the split tile this CTA finishes next,
+    // fetched when its segment starts if they have all counted in by then
+    // (up to 16 columns a worker; wider tiles fetch it at the epilogue)
+    float pre[kCols] = {};
+    bool pre_ok = false;
     // both accumulators start at zero
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl) tmem_zero_cols<kCols>(tbase + lane_base + sl * C::kDCols + c0);
@@ -1008,7 +1035,41 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[rs.slot]);
         rs.next();
-        finish_segment<QUANT, TPAD>(epi, (int)ptile, (prec & kStageWhole) != 0, v, p, m, c0, wk, lane);
+        if (!finish_segment<QUANT, TPAD>(epi, (int)ptile, (prec & kStageWhole) != 0, (prec & kStageFrom0) != 0, v,
+                                         pre, pre_ok, p, m, c0, wk, lane, ctl)) {
+          ok = false;
+          break;
+        }
+      }
+      if (kCols <= 16 && has_d && (rec & kStageFinStart)) {
+        // this stage starts the segment that finishes a split tile: if the
+        // other contributors have all counted in, fetch their sum now, so
+        // that it lands while this segment's MMAs run
+        if (!pdl_done) {
+          // split-tile sums and counters may still be used by the previous kernel
+          pdl_wait_prior();
+          pdl_done = true;
+        }
+        const int e = (int)(rec & 0xFFFFu);
+        const int U = E[e].units, ks = E[e].ks;
+        const int need = cta_of_unit((int)tile * ks + ks - 1, U, G) - cta;
+        const size_t key = (size_t)(e % kSplitKeys) * p.slot_ctas + cta;
+        int ready = 0;
+        if (lane == 0) ready = ld_acquire_gpu(p.split_cnt + key * kGemmWorkers + wk) >= need;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        __syncwarp();   // orders lane 0's acquire before the other lanes' reads
+        if (ready) {
+          const float* slot = p.partials + (key * kTileM + m) * TPAD + c0;
+#pragma unroll
+          for (int c = 0; c < kCols; c += 4) {
+            const float4 s4 = ldcg_f32x4(slot + c);
+            pre[c] = s4.x;
+            pre[c + 1] = s4.y;
+            pre[c + 2] = s4.z;
+            pre[c + 3] = s4.w;
+          }
+          pre_ok = true;
+        }
       }
       if (!has_d) break;
       prec = rec;

@@ -15,11 +15,14 @@ time per step (GB/s) with inputs resident; `e2e` is the same metric when
 every step also copies its inputs from pinned host memory (double-buffered
 against the previous step's compute) and reads its result back.  Sub-objects
 time, each on its own graph: `t16` (the stack at T = 16 without head and
-acceptance), `w8_27b` (the 27B-class int8 stack with rotation),
+acceptance), `t16_unfused` (seven GEMMs per layer), `per_gemm_launches`
+(one launch per GEMM), `w4_rot32` (the T = 32 stack with the block-32
+rotation), `w8_27b` (the 27B-class int8 stack with rotation),
 `accept_gumbel` (shared-seed acceptance of the same blocks) and `accept_tree`
-(greedy trees of 32 and 64 nodes).  `--impl reference` times the fp64 CPU
+(greedy trees of 1 to 64 nodes).  `--impl reference` times the fp64 CPU
 oracle on a bounded sample instead; `--kernel-case`, `--kernel-case-w8`,
-`--accept-case`, `--gumbel-case` and `--tree-case` time one kernel alone.
+`--stack-case`, `--accept-case`, `--gumbel-case` and `--tree-case` time one
+kernel alone.
 """
 from __future__ import annotations
 
@@ -404,6 +407,16 @@ def run_gpu(args):
     pg_ms = time_graph(g_pg, max(5, min(K, 20)))
     del g_pg
 
+    # ---- the same T=32 stack (36 layers + LM head) with the block-32 random
+    # Hadamard rotation of every GEMM's activations inside the launch
+    s32 = {k_: torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(400 + k_), k_)).to(dev)
+           for k_ in sorted({k for _, k, _ in inputs.LAYER_9B} | {HIDDEN})}
+    st32r = sv.GemmStack(ctx, [dict(d, signs=s32[d["K"]], hadamard_block=32)
+                               for d in stack_descs(T_MAIN, xs, x_head, True)])
+    g_r32 = graph_of(st32r.run)
+    r32_ms = time_graph(g_r32, max(5, min(K, 20)))
+    del g_r32, st32r
+
     # ---- config 1 as stated: q, k, v, o, gate, up, down as seven GEMMs per
     # layer at T=16 (q/k/v share their input, so k and v do not wait for q; up
     # does not wait for gate).  The codes are row ranges of the fused
@@ -670,6 +683,17 @@ def run_gpu(args):
                 "value": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
                 "frac": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9 / peak, 4),
+            },
+            "w4_rot32": {
+                "workload": "the T=32 verify GEMM stack (36 layers + LM head, one launch) with the "
+                            "block-32 random Hadamard rotation of every GEMM's activations inside "
+                            "the launch",
+                "ms_per_step": round(r32_ms, 5),
+                "value": round(gemm_bytes / (r32_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
+                "frac": round(gemm_bytes / (r32_ms * 1e-3) / 1e9 / peak, 4),
+                "without_rotation_ms": round(gemm_ms, 5),
+                "rotation_overhead": round(r32_ms / gemm_ms - 1.0, 4),
             },
             "w8_27b": {
                 "workload": "27B-class int8 per-channel stack at T=32: 64 layers (qkv 5120x7168, "

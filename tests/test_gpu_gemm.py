@@ -104,6 +104,38 @@ def test_w4_with_rotation_parity(ctx):
     assert gemm_error_ratio(y, ref, False) <= 1.0
 
 
+@pytest.mark.parametrize("T", [16, 32])
+def test_w4_block32_rotation_parity(ctx, T):
+    # the smallest Hadamard block (32): one warp lane per element, no
+    # in-register butterfly levels; ragged N and several 256-k stages
+    rng = np.random.default_rng(3200 + T)
+    N, K, B = 1056, 4096, 32
+    W = inputs.w4_weights(rng, N, K, 64)
+    xb = inputs.activations(rng, T, K)
+    s = inputs.hadamard_signs(rng, K)
+    for f32 in (True, False):
+        y = _run_w4(ctx, W, xb, T, f32, s, B)
+        ref = oracle.qgemm_w4a16(W.qcodes, W.scales, W.zeros, 64, xb, T, N, K, s, B)
+        assert gemm_error_ratio(y, ref, not f32) <= 1.0
+
+
+def test_w4_block32_rotation_full_size_sampled(ctx):
+    # the 9B-class fused gate/up projection with the block-32 rotation
+    rng = np.random.default_rng(3300)
+    T, N, K, B = 32, 24576, 4096, 32
+    W = inputs.w4_weights(rng, N, K, 64, keep_raw=False)
+    xb = inputs.activations(rng, T, K)
+    s = inputs.hadamard_signs(rng, K)
+    y = _run_w4(ctx, W, xb, T, True, s, B)
+    rows = np.sort(rng.choice(N // 2, size=64, replace=False))
+    rows = np.stack([2 * rows, 2 * rows + 1], axis=1).reshape(-1)
+    pairs = rows[0::2] // 2
+    ref = oracle.qgemm_w4a16(W.qcodes[rows], W.scales[:, rows], W.zeros[:, pairs], 64, xb, T, len(rows), K,
+                             s, B)
+    assert np.isfinite(y).all()
+    assert gemm_error_ratio(y[:, rows], ref, False) <= 1.0
+
+
 def test_w4_integer_special_case_is_exact(ctx):
     # zero points 0, scales 1, small integer activations: every partial sum
     # is an integer below 2^24, so the GPU result must be exact.
@@ -120,8 +152,8 @@ def test_w4_integer_special_case_is_exact(ctx):
 
 
 def test_counters_and_slots_reset_between_calls(ctx):
-    # Split tiles are summed in a shared fp32 slot that the last contributor
-    # clears; a different shape in between must not see stale sums.
+    # Split tiles are summed in a shared fp32 slot that the CTA finishing the
+    # tile clears; a different shape in between must not see stale sums.
     rng = np.random.default_rng(6)
     A = inputs.w4_weights(rng, 2048, 2048, 64)
     B = inputs.w4_weights(rng, 1056, 768, 64)

@@ -951,9 +951,10 @@ def run_kernel_case_w8(args):
 
 def run_stack_case(args):
     """One GEMM stack alone, graph-replayed warm-up + steps times: `9b32[:L]`
-    (L layers of the T=32 int4 stack plus the LM head), `9b16[:L]` (the T=16
-    stack), `27b[:L]` / `27bnr[:L]` (the int8 Large-tier stack with / without
-    rotation).  L defaults to the full depth.  Prints device time per launch
+    (L layers of the T=32 int4 stack plus the LM head), `9b32r32[:L]` (the same
+    with the block-32 rotation of every GEMM's activations), `9b16[:L]` (the
+    T=16 stack), `27b[:L]` / `27bnr[:L]` (the int8 Large-tier stack with /
+    without rotation).  L defaults to the full depth.  Prints device time per launch
     and bandwidth."""
     import numpy as np
     import torch
@@ -967,8 +968,11 @@ def run_stack_case(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(11)
     descs, keep, nbytes = [], [], 0
-    if name in ("9b32", "9b16"):
-        T = 32 if name == "9b32" else 16
+    if name in ("9b32", "9b32r32", "9b16"):
+        T = 16 if name == "9b16" else 32
+        rot = name == "9b32r32"
+        sgn = {k: torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(400 + k), k)).to(dev)
+               for k in sorted({k for _, k, _ in inputs.LAYER_9B} | {HIDDEN})}
         L = int(depth) if depth else inputs.LAYERS_9B
         ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _, _, N in inputs.LAYER_9B]
         for _ in range(L):
@@ -978,16 +982,18 @@ def run_stack_case(args):
                 keep += [w, x]
                 descs.append({"quant": sv.SPEC_QUANT_W4, "qcodes": w["qcodes"], "scales": w["scales"],
                               "zeros": w["zeros"], "group_size": GROUP, "x": x, "y": ys[j], "T": T,
-                              "N": N, "K": K, "wait_prev": 1})
+                              "N": N, "K": K, "wait_prev": 1,
+                              "signs": sgn[K] if rot else None, "hadamard_block": 32 if rot else 0})
                 nbytes += w4_gemm_bytes(T, N, K)
-        if name == "9b32":
+        if name != "9b16":
             w = inputs.w4_weights_device(gen, VOCAB, HIDDEN, dev, GROUP)
             x = inputs.activations_device(gen, T, HIDDEN, dev)
             y = torch.empty((T, VOCAB), dtype=torch.float32, device=dev)
             keep += [w, x, y]
             descs.append({"quant": sv.SPEC_QUANT_W4, "qcodes": w["qcodes"], "scales": w["scales"],
                           "zeros": w["zeros"], "group_size": GROUP, "x": x, "y": y, "T": T,
-                          "N": VOCAB, "K": HIDDEN, "wait_prev": 1})
+                          "N": VOCAB, "K": HIDDEN, "wait_prev": 1,
+                          "signs": sgn[HIDDEN] if rot else None, "hadamard_block": 32 if rot else 0})
             nbytes += head_bytes(T)
     else:
         rot = name == "27b"

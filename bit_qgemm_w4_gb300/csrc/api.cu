@@ -158,6 +158,8 @@ int check_rotation(const int8_t* signs, int block, int T, int K) {
   if (block < 32 || block > 1024 || (block & (block - 1)))
     return set_error(SPEC_ERR_SHAPE, "hadamard_block %d not a power of two in [32, 1024]", block);
   if (K % block) return set_error(SPEC_ERR_SHAPE, "K=%d not a multiple of hadamard_block %d", K, block);
+  if (reinterpret_cast<uintptr_t>(signs) % 16)
+    return set_error(SPEC_ERR_ARG, "signs must be 16-byte aligned");
   if (K > kMaxK || 2 * T > kMaxT)
     return set_error(SPEC_ERR_SHAPE, "rotated GEMMs take T <= %d, K <= %d", kMaxT / 2, kMaxK);
   return SPEC_OK;

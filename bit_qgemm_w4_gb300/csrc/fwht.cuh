@@ -131,6 +131,69 @@ __device__ __forceinline__ void fwht_warp(const uint16_t* x, uint16_t* y, const 
   }
 }
 
+// One thread's rotation of one small block (B = 32): the whole block in
+// registers, the log2(B) butterfly levels without shuffles, the same output
+// forms as fwht_warp.  Used where there are many small blocks, so that a
+// warp rotates 32 blocks at once instead of one.  signs must be 16-byte
+// aligned.
+template <int B, int MODE>
+__device__ __forceinline__ void fwht_thread(const uint16_t* x, uint16_t* y, const int8_t* signs,
+                                            float scale, size_t split_stride = 0) {
+  static_assert(B % 16 == 0, "whole 16-byte loads");
+  float v[B];
+#pragma unroll
+  for (int r = 0; r < B; r += 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(x + r);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[r + 2 * j] = fwht_bf16_to_f32(ws[j] & 0xFFFFu);
+      v[r + 2 * j + 1] = fwht_bf16_to_f32(ws[j] >> 16);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < B; r += 16) {
+    const uint4 sg = *reinterpret_cast<const uint4*>(signs + r);
+    const uint32_t sw[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if ((sw[j >> 2] >> (8 * (j & 3) + 7)) & 1u) v[r + j] = -v[r + j];
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < B; h <<= 1) {
+#pragma unroll
+    for (int r = 0; r < B; ++r) {
+      if ((r & h) == 0) {
+        const float a = v[r], c = v[r + h];
+        v[r] = a + c;
+        v[r + h] = a - c;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < B; ++r) {
+    v[r] *= scale;
+    if (MODE == kFwhtF16Nib && fwht_nib(r)) v[r] *= 0.0625f;
+  }
+  auto enc = [](float f) { return MODE >= kFwhtF16Nib ? fwht_f32_to_f16(f) : fwht_f32_to_bf16(f); };
+#pragma unroll
+  for (int r = 0; r < B; r += 8) {
+    uint32_t ws[4], wl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t a = enc(v[r + 2 * j]), b = enc(v[r + 2 * j + 1]);
+      ws[j] = a | (b << 16);
+      if (MODE == kFwhtBf16Split)
+        wl[j] = fwht_f32_to_bf16(v[r + 2 * j] - fwht_bf16_to_f32(a)) |
+                (fwht_f32_to_bf16(v[r + 2 * j + 1] - fwht_bf16_to_f32(b)) << 16);
+    }
+    *reinterpret_cast<uint4*>(y + r) = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    if (MODE == kFwhtBf16Split)
+      *reinterpret_cast<uint4*>(y + split_stride + r) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
+}
+
 // Runtime block size B in {32, 64, ..., 1024}.
 template <int MODE>
 __device__ __forceinline__ void fwht_warp_any(int B, const uint16_t* x, uint16_t* y,

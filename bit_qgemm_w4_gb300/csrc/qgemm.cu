@@ -722,7 +722,25 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         const int K = en.K, kind = en.kind;
         const uint16_t* x = en.x;
         uint16_t* xp = en.xprep;
-        if (en.prep == 1) {
+        if (en.prep == 1 && en.rot_block == 32) {
+          // rotation, 32-element blocks: one lane per (row, block), the
+          // block in its registers (a warp rotates 32 blocks at once)
+          const int8_t* signs = en.signs;
+          const float rscale = en.rot_scale;
+          const int nblk = K / 32;
+          const int pairs = en.T * nblk;
+          for (int pp = cta * 32 + lane; pp < pairs; pp += G * 32) {
+            const int t = pp / nblk, b = pp - t * nblk;
+            const size_t col = (size_t)b * 32;
+            const uint16_t* xs = x + (size_t)t * K + col;
+            if (kind == kGemmBf16)
+              fwht_thread<32, kFwhtBf16Split>(xs, xp + (size_t)(2 * t) * K + col, signs + col, rscale, (size_t)K);
+            else if (kind == kGemmF16Nib)
+              fwht_thread<32, kFwhtF16Nib>(xs, xp + (size_t)t * K + col, signs + col, rscale);
+            else
+              fwht_thread<32, kFwhtF16>(xs, xp + (size_t)t * K + col, signs + col, rscale);
+          }
+        } else if (en.prep == 1) {
           // rotation: one warp per (row, block)
           const int B = en.rot_block;
           const int8_t* signs = en.signs;

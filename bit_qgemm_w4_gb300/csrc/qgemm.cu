@@ -96,9 +96,12 @@ struct Cfg {
   static constexpr int kXSlots = kXSlot > 16384 ? 2 : 4;
   static constexpr int kCtrl = 1024;
   static constexpr int kSmemBudget = 225 * 1024;
-  static constexpr int kWSlotsFit = (kSmemBudget - 1024 - kCtrl - kXSlots * kXSlot) / kWSlot;
+  // the split-tile sum a CTA finishes, fetched early into shared memory
+  // ([128 rows][TPAD] fp32) where a worker reads at most 16 columns
+  static constexpr int kPreBytes = TPAD / 2 <= 16 ? kTileM * TPAD * 4 : 0;
+  static constexpr int kWSlotsFit = (kSmemBudget - 1024 - kCtrl - kXSlots * kXSlot - kPreBytes) / kWSlot;
   static constexpr int kWSlots = kWSlotsFit > 12 ? 12 : kWSlotsFit;
-  static constexpr int kSmemBytes = 1024 + kXSlots * kXSlot + kWSlots * kWSlot + kCtrl;
+  static constexpr int kSmemBytes = 1024 + kXSlots * kXSlot + kWSlots * kWSlot + kPreBytes + kCtrl;
   // TMEM: two accumulators of TPAD columns (a CTA's consecutive tile
   // segments alternate between them; every MMA warp adds into the current
   // one), then from column 128 a ring of A slots (one stage each, 32 columns
@@ -129,7 +132,7 @@ struct Cfg {
   static_assert(kCols % 8 == 0, "epilogue columns in multiples of 8");
   static constexpr int kDM = 4;                                 // ring of per-stage "MMAs done" barriers
   static_assert(kNA <= kDM && kXSlots <= kDM, "a slot is reused within the done ring");
-  static_assert((2 * kWSlots + 3 * kXSlots + kNA + kDM + 4) * 8 + 8 <= kCtrl, "barrier block");
+  static_assert((2 * kWSlots + 3 * kXSlots + kNA + kDM + 4 + kGemmWorkers) * 8 + 8 <= kCtrl, "barrier block");
 };
 
 struct Params {
@@ -422,13 +425,13 @@ struct EpiEntry {
 // CTA holding its first k, whose share is the last segment of its range and
 // so, in time, usually the last to complete): every other contributor adds
 // its part into the tile's fp32 slot and counts itself in with a release;
-// the finisher adds the slot's sum (fetched early into `pre` when the
-// others had already counted in, else waited for here) to its own part.
-// False when that wait gives up (abort or time limit).
+// the finisher adds the slot's sum (already in shared memory at `pre_row`
+// when the others had counted in by the time its segment started, else
+// waited for and read here) to its own part.  False when that wait gives up
+// (abort or time limit).
 template <int QUANT, int TPAD>
 __device__ __forceinline__ bool finish_segment(const EpiEntry& en, int tile, bool whole, bool from0,
-                                            float (&v)[Cfg<QUANT, TPAD>::kCols],
-                                            float (&pre)[Cfg<QUANT, TPAD>::kCols], bool& pre_ok,
+                                            float (&v)[Cfg<QUANT, TPAD>::kCols], const float* pre_row,
                                             const Params& p, int m, int c0, int wk, int lane,
                                             const Ctl& ctl) {
   constexpr int kCols = Cfg<QUANT, TPAD>::kCols;
@@ -454,7 +457,17 @@ __device__ __forceinline__ bool finish_segment(const EpiEntry& en, int tile, boo
       __syncwarp();
       if (lane == 0) red_release_gpu_add(cnt, 1);
     } else {
-      if (!pre_ok) {
+      float pre[kCols];
+      if (pre_row) {
+#pragma unroll
+        for (int c = 0; c < kCols; c += 4) {
+          const float4 s4 = *reinterpret_cast<const float4*>(pre_row + c);
+          pre[c] = s4.x;
+          pre[c + 1] = s4.y;
+          pre[c + 2] = s4.z;
+          pre[c + 3] = s4.w;
+        }
+      } else {
         int ready = 1;
         if (lane == 0) ready = wait_count(cnt, c_last - c_first, ctl) ? 1 : 0;
         ready = __shfl_sync(0xffffffffu, ready, 0);
@@ -469,7 +482,6 @@ __device__ __forceinline__ bool finish_segment(const EpiEntry& en, int tile, boo
           pre[c + 3] = s4.w;
         }
       }
-      pre_ok = false;
 #pragma unroll
       for (int c = 0; c < kCols; ++c) v[c] += pre[c];
 #pragma unroll
@@ -542,7 +554,8 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
                                              ~uintptr_t(1023));
   uint8_t* xreg = smem;
   uint8_t* wreg = smem + SX * C::kXSlot;
-  uint8_t* ctrl = wreg + SW * C::kWSlot;
+  float* pre_s = reinterpret_cast<float*>(wreg + SW * C::kWSlot);
+  uint8_t* ctrl = wreg + SW * C::kWSlot + C::kPreBytes;
   uint64_t* wfull = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* wempty = wfull + SW;
   uint64_t* xfull = wempty + SW;
@@ -558,7 +571,9 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
   // xrec[s]: the control record of the stage in activation slot s (written
   // by the activation producer before the slot's copies)
   uint2* xrec = reinterpret_cast<uint2*>(xconv + SX);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xrec + SX);
+  // prebar[w]: worker w's part of an early-fetched split-tile sum has landed
+  uint64_t* prebar = reinterpret_cast<uint64_t*>(xrec + SX);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(prebar + kGemmWorkers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const GemmEntry* E = p.entries ? p.entries : &e0;
@@ -579,6 +594,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     }
     for (int s = 0; s < NA; ++s) mbar_init(&afull[s], kGemmWorkers);
     for (int s = 0; s < C::kDM; ++s) mbar_init(&mdone[s], C::kMmaW);   // one commit per MMA warp
+    for (int s = 0; s < kGemmWorkers; ++s) mbar_init(&prebar[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sfull[s], C::kMmaW);
       mbar_init(&sempty[s], kGemmWorkers);
@@ -953,11 +969,13 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     bool ok = true, pdl_done = false;
     bool more = last_entry_of(E, nE, G, cta) >= 0;   // this CTA owns any stage
     uint32_t prec = 0, ptile = 0;                     // the previous stage's control record
-    // the other contributors' sum of the split tile this CTA finishes next,
-    // fetched when its segment starts if they have all counted in by then
-    // (up to 16 columns a worker; wider tiles fetch it at the epilogue)
-    float pre[kCols] = {};
+    // the other contributors' sum of the split tile this CTA finishes next
+    // is copied into shared memory when that segment starts, if they have
+    // all counted in by then (up to 16 columns a worker; wider tiles read it
+    // at the epilogue)
     bool pre_ok = false;
+    uint32_t pre_phase = 0;
+    const float* pre_row = C::kPreBytes ? pre_s + (size_t)m * TPAD + c0 : nullptr;
     // both accumulators start at zero
 #pragma unroll
     for (int sl = 0; sl < 2; ++sl) tmem_zero_cols<kCols>(tbase + lane_base + sl * C::kDCols + c0);
@@ -1053,13 +1071,23 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[rs.slot]);
         rs.next();
+        const bool fin = (prec & (kStageWhole | kStageFrom0)) == kStageFrom0;
+        const bool use_pre = fin && pre_ok;
+        if (use_pre) {
+          if (!wait_warp(&prebar[wk], pre_phase, ctl)) {
+            ok = false;
+            break;
+          }
+          pre_phase ^= 1u;
+          pre_ok = false;
+        }
         if (!finish_segment<QUANT, TPAD>(epi, (int)ptile, (prec & kStageWhole) != 0, (prec & kStageFrom0) != 0, v,
-                                         pre, pre_ok, p, m, c0, wk, lane, ctl)) {
+                                         use_pre ? pre_row : nullptr, p, m, c0, wk, lane, ctl)) {
           ok = false;
           break;
         }
       }
-      if (kCols <= 16 && has_d && (rec & kStageFinStart)) {
+      if (C::kPreBytes && has_d && (rec & kStageFinStart)) {
         // this stage starts the segment that finishes a split tile: if the
         // other contributors have all counted in, fetch their sum now, so
         // that it lands while this segment's MMAs run
@@ -1077,15 +1105,19 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         ready = __shfl_sync(0xffffffffu, ready, 0);
         __syncwarp();   // orders lane 0's acquire before the other lanes' reads
         if (ready) {
-          const float* slot = p.partials + (key * kTileM + m) * TPAD + c0;
-#pragma unroll
-          for (int c = 0; c < kCols; c += 4) {
-            const float4 s4 = ldcg_f32x4(slot + c);
-            pre[c] = s4.x;
-            pre[c + 1] = s4.y;
-            pre[c + 2] = s4.z;
-            pre[c + 3] = s4.w;
+          // one bulk copy per row of this warp's part, issued by lane 0
+          // after its acquire (the async proxy reads what the acquire made
+          // visible; this warp's earlier reads of the buffer come first)
+          if (lane == 0) {
+            fence_proxy_async_global();
+            fence_proxy_async_smem();
+            const int r0 = (warp & 3) * 32;
+            mbar_arrive_expect_tx(&prebar[wk], (uint32_t)(32 * kCols * 4));
+            for (int r = 0; r < 32; ++r)
+              bulk_g2s(pre_s + (size_t)(r0 + r) * TPAD + c0,
+                       p.partials + ((key * kTileM + r0 + r) * TPAD + c0), (uint32_t)(kCols * 4), &prebar[wk]);
           }
+          __syncwarp();
           pre_ok = true;
         }
       }
@@ -1097,6 +1129,8 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       tmem_wait_st();
       tmem_wait_ld();
     }
+    // a split-tile sum still being copied in lands before the CTA exits
+    if (pre_ok && lane == 0) drain_bar(&prebar[wk], pre_phase);
   }
 
   tc_fence_before();

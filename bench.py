@@ -949,6 +949,41 @@ def run_kernel_case_w8(args):
     ctx.close()
 
 
+def run_fwht_case(args):
+    """The standalone rotation fwht_rotate on a T x K bf16 block (block size
+    B) launched warm-up + steps times; prints its device time and the
+    bandwidth of its 4*T*K bytes (bf16 in and out)."""
+    import numpy as np
+    import torch
+
+    import bit_qgemm_w4_gb300 as sv
+    from bit_qgemm_w4_gb300 import build as svbuild
+    svbuild.build()
+    T, K, B = [int(v) for v in args.fwht_case.split(",")]
+    dev = torch.device("cuda", 0)
+    ctx = sv.Context(0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(13)
+    x = inputs.activations_device(gen, T, K, dev)
+    y = torch.empty_like(x)
+    signs = torch.from_numpy(inputs.hadamard_signs(np.random.default_rng(5), K)).to(dev)
+    for _ in range(args.warmup):
+        sv.fwht_rotate(ctx, x, y, T, K, signs, B)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        sv.fwht_rotate(ctx, x, y, T, K, signs, B)
+    e1.record()
+    torch.cuda.synchronize()
+    sv.spec_sync_status(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = 4 * T * K
+    print(json.dumps({"fwht_case": [T, K, B], "ms_per_launch": round(ms, 6),
+                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes}), flush=True)
+    ctx.close()
+
+
 def run_stack_case(args):
     """One GEMM stack alone, graph-replayed warm-up + steps times: `9b32[:L]`
     (L layers of the T=32 int4 stack plus the LM head), `9b32r32[:L]` (the same
@@ -1176,7 +1211,9 @@ def main():
     ap.add_argument("--kernel-case-w8", default=None, metavar="T,N,K[,B]",
                     help="time one per-channel int8 GEMM shape (B > 0: rotation block)")
     ap.add_argument("--stack-case", default=None, metavar="NAME[:LAYERS]",
-                    help="time one GEMM stack alone: 9b32, 9b16, 27b or 27bnr, optionally fewer layers")
+                    help="time one GEMM stack alone: 9b32, 9b32r32, 9b16, 27b or 27bnr, optionally fewer layers")
+    ap.add_argument("--fwht-case", default=None, metavar="T,K,B",
+                    help="time the standalone rotation on a T x K block")
     ap.add_argument("--kernel-case", default=None, metavar="T,N,K",
                     help="time one int4 GEMM shape in isolation instead of the verify step")
     args = ap.parse_args()
@@ -1194,6 +1231,9 @@ def main():
         return
     if args.stack_case:
         run_stack_case(args)
+        return
+    if args.fwht_case:
+        run_fwht_case(args)
         return
     if args.kernel_case:
         run_kernel_case(args)

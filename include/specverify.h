@@ -105,19 +105,18 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  *   y[t][n] = sum_k x'[t][k] * (code[n][k] - zero[k/g][n]) * scale[k/g][n]
  * x' = x, or, when signs != NULL and hadamard_block > 0, the block random
  * Hadamard rotation of x (see fwht_rotate; the weights are taken as stored
- * already rotated).  The rotation runs inside the same launch, in fp32, and
- * its result enters the tensor cores as the sum of two bf16 values (the
- * rounded value and its remainder), so it adds no bf16 rounding; it uses the
- * context's rotation scratch.
- * Sizes: 1 <= T <= 64 (T <= 32 with rotation); N % 32 == 0; K % 64 == 0;
- * group_size a power of two >= 64 with K % group_size == 0.  y_dtype is
- * SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
- * Numerics: the tensor cores multiply the exact integers (code - zero),
- * held in bf16, by the bf16 activations as given, and sum each 64-k block in
- * fp32; the block's fp16 scale is then applied in fp32 and the blocks are
- * added in fp32.  Nothing is rounded before the sums, so the result differs
- * from the exact product sum only by fp32 rounding of the additions (and the
- * final rounding of a bf16 output).  Any finite bf16 activation is valid. */
+ * already rotated).  The rotation runs inside the same launch, in fp32, with
+ * one rounding of its result to fp16; signs must then be 16-byte aligned.
+ * Sizes: 1 <= T <= 64 (T <= 32 with rotation); N % 32 == 0; K % 64 == 0,
+ * K <= 32768; group_size a power of two >= 64 with K % group_size == 0.
+ * y_dtype is SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
+ * Numerics: each weight (code - zero) * scale is rounded once to fp16 (the
+ * difference is exact, the product rounded); the activations enter the
+ * tensor cores as fp16 (bf16 magnitudes from 2^-10 to 65504 convert
+ * exactly; smaller ones round to fp16's subnormal grid, larger ones become
+ * infinite); the products are summed in fp32.  The result's error is that of the fp16
+ * weights, about 1e-3 * RMS(y) at its largest over 10^6 outputs, plus fp32
+ * summation and the final rounding of a bf16 output. */
 int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
                 const uint8_t* zeros, int group_size, const uint16_t* x, void* y,
                 int y_dtype, int T, int N, int K, const int8_t* signs,
@@ -127,10 +126,14 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
  * checkpoint, 8-bit symmetric quantisation, no zero point).
  *   y[t][n] = sum_k x'[t][k] * code[n][k] * scale
  * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size a
- * power of two >= 64).  The int8 codes enter the tensor cores exactly (bf16
- * holds -127..127); a per-channel scale multiplies the fp32 sum, grouped
- * scales each 64-k block's fp32 sum, as in qgemm_w4a16.  Rotation and sizes
- * as qgemm_w4a16, except N % 8 == 0 suffices. */
+ * power of two >= 64).  Per-channel scales: the int8 codes enter the tensor
+ * cores exactly (bf16 holds -127..127) with the bf16 activations as given,
+ * and the scale multiplies the fp32 sum; a rotated activation enters as the
+ * sum of two bf16 values (the rounded value and its remainder), so the
+ * rotation adds no bf16 rounding.  Grouped scales: code * scale rounded once
+ * to fp16 and fp16 activations, as in qgemm_w4a16.  Rotation and sizes as
+ * qgemm_w4a16, except N % 8 == 0 suffices and per-channel K may reach 2^20
+ * (32768 with rotation). */
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, const uint16_t* x, void* y, int y_dtype, int T,
                 int N, int K, const int8_t* signs, int hadamard_block,
@@ -172,8 +175,7 @@ typedef struct spec_gemm_stack spec_gemm_stack;
  * descriptors' pointers and sizes are fixed from then on (the tensors must
  * stay allocated while the stack is used).  Rules beyond each GEMM's own:
  * one quant for all entries; at most 3 consecutive entries (after the
- * first) with wait_prev = 0; a rotated entry after another rotated entry
- * needs wait_prev = 1 (rotated GEMMs share the context's rotation scratch).
+ * first) with wait_prev = 0.
  * The stack holds a small device array (cudaMalloc at creation) and belongs
  * to `ctx`.  qgemm_stack_run enqueues the whole stack on `stream` (one
  * kernel launch; a launch may be captured in a CUDA graph); the results are

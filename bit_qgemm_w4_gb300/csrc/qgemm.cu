@@ -70,6 +70,7 @@ constexpr uint32_t kStageWhole = 1u << 17;    // ... and it covered the whole ti
 constexpr uint32_t kStageLast = 1u << 18;     // the CTA's last stage of the launch
 constexpr uint32_t kStageFrom0 = 1u << 19;    // (at a segment end) the segment began at the tile's first k
 constexpr uint32_t kStageFinStart = 1u << 20; // first stage of a segment that finishes a split tile
+constexpr int kStageConvShift = 21;           // (activation records) the GEMM's xconv mode, 2 bits
 
 template <int QUANT, int TPAD>
 struct Cfg {
@@ -631,9 +632,15 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       const CUtensorMap *codes = nullptr, *scales = nullptr, *zeros = nullptr;
       uint32_t tx = 0;
       int rows = 0, gshift = 0;
-      __device__ __forceinline__ void at(const GemmEntry* E, int e_) {
+      __device__ __forceinline__ void at(const GemmEntry* E, int nE, int e_, bool lead) {
         if (e_ == e) return;
         e = e_;
+        if (lead && e + 1 < nE) {
+          // the next GEMM's descriptors, so that its first copies do not wait for them
+          prefetch_tensormap(&E[e + 1].tm_codes);
+          prefetch_tensormap(&E[e + 1].tm_scales);
+          prefetch_tensormap(&E[e + 1].tm_zeros);
+        }
         codes = &E[e].tm_codes;
         scales = &E[e].tm_scales;
         zeros = &E[e].tm_zeros;
@@ -651,7 +658,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     const int last_e = last_entry_of(E, nE, G, cta);
     bool from0 = false;
     auto prefetch_next = [&]() {
-      spf.at(E, pf.e);
+      spf.at(E, nE, pf.e, false);
       if (leader) {
         tma_prefetch_2d(spf.codes, pf.kst * 128, pf.tile * kTileM);
         if (spf.rows) {
@@ -676,7 +683,7 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         skipped = n;   // test hook: this stage's weights never arrive
         continue;
       }
-      sw.at(E, w.e);
+      sw.at(E, nE, w.e, leader);
       const bool seg_start = w.kst == 0 || w.u == w.ub;
       if (seg_start) from0 = w.kst == 0;
       const bool seg_end = w.kst == w.ks - 1 || w.u == w.ue - 1;
@@ -720,6 +727,21 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
       const GemmEntry& en = E[e];
       const int ub = unit_begin(cta, en.units, G), ue = unit_begin(cta + 1, en.units, G);
       const bool gate = p.gate && en.wait_prev && e > 0;
+      if (ub < ue && lane == 0) {
+        // while the gate is closed: the GEMM's activation descriptor, and
+        // (activations read as given) its first boxes into L2 -- a hint
+        // only, still correct if an earlier GEMM writes them meanwhile
+        prefetch_tensormap(&en.tm_x);
+        if (!en.prep) {
+          const int ks0 = en.ks;
+          int k0 = ub % ks0;
+          for (int u = ub; u < ue && u < ub + SX; ++u) {
+#pragma unroll
+            for (int j = 0; j < SUB; ++j) tma_prefetch_2d(&en.tm_x, k0 * C::kStageKK + kGroupK * j, 0);
+            if (++k0 == ks0) k0 = 0;
+          }
+        }
+      }
       if (gate && (en.prep || ub < ue)) {
         // this GEMM reads what the earlier ones wrote: wait until every one
         // of their tiles is finished
@@ -797,8 +819,9 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
         break;
       }
       if (gate || en.prep) fence_proxy_async_global();
-      if (lane == 0) prefetch_tensormap(&en.tm_x);
       const CUtensorMap* tmx = &en.tm_x;
+      const uint32_t xmode = (uint32_t)en.xconv << kStageConvShift;
+      const uint32_t xidesc = en.idesc;
       const int ks = en.ks;
       int kst = ub % ks;
       for (int u = ub; u < ue; ++u, r.next(), ++n) {
@@ -813,8 +836,8 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
           uint8_t* st = xreg + r.slot * C::kXSlot;
           const bool seg_end = kst == ks - 1 || u == ue - 1;
           xrec[r.slot] = make_uint2((uint32_t)e | (seg_end ? kStageSegEnd : 0u) |
-                                        (e == last_e && u == ue - 1 ? kStageLast : 0u),
-                                    0u);
+                                        (e == last_e && u == ue - 1 ? kStageLast : 0u) | xmode,
+                                    xidesc);
           mbar_arrive_expect_tx(&xfull[r.slot], (uint32_t)(SUB * C::kXBox));
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
@@ -833,14 +856,11 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     // final barrier)
     if (C::kConv0 == 2 && (p.prep_flags & kAnyConv)) {
       Ring<SX> r;
-      int ce = -1, mode = 0;
+      int mode = 0;
       for (bool more = last_entry_of(E, nE, G, cta) >= 0; more; r.next()) {
         if (!wait_warp(&xfull[r.slot], r.phase, ctl)) break;
         const uint32_t rec = xrec[r.slot].x;
-        if ((int)(rec & 0xFFFFu) != ce) {
-          ce = (int)(rec & 0xFFFFu);
-          mode = E[ce].xconv;
-        }
+        mode = (int)((rec >> kStageConvShift) & 3u);
         convert_share<C>(mode, xreg + r.slot * C::kXSlot, &xconv[r.slot], warp - C::kConv0, lane);
         if (rec & kStageLast) more = false;
       }
@@ -857,19 +877,17 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     Ring<SX> rx;
     Ring<C::kDM> rm;
     Ring<2> rs;
-    int ce = -1, last_m = -1, xconv_mode = 0;
+    int last_m = -1, xconv_mode = 0;
     const bool any_conv = (p.prep_flags & kAnyConv) != 0;
     uint32_t idesc = 0, last_mph = 0;
     bool seg_start = true;
     for (bool more = last_entry_of(E, nE, G, cta) >= 0; more;) {
       // the stage's activations (and its control record) have landed
       if (!wait_warp(&xfull[rx.slot], rx.phase, ctl)) break;
-      const uint32_t rec = xrec[rx.slot].x;
-      if ((int)(rec & 0xFFFFu) != ce) {
-        ce = (int)(rec & 0xFFFFu);
-        idesc = E[ce].idesc;
-        xconv_mode = E[ce].xconv;
-      }
+      const uint2 xr = xrec[rx.slot];
+      const uint32_t rec = xr.x;
+      idesc = xr.y;
+      xconv_mode = (int)((rec >> kStageConvShift) & 3u);
       if (any_conv) convert_share<C>(xconv_mode, xreg + rx.slot * C::kXSlot, &xconv[rx.slot], warp - C::kConv0, lane);
       // a segment starts on a zeroed accumulator (zeroed at the start of the
       // launch, then by the workers after they read it)
@@ -926,6 +944,12 @@ __global__ void __maxnreg__((Cfg<QUANT, TPAD>::kMaxRegs))
     EpiEntry epi{};
     auto enter_d = [&](int e) {
       ed = e;
+      if (p.entries) {
+        // the fields the epilogue reads for this GEMM, into L1 ahead of it
+        const uint8_t* fe = reinterpret_cast<const uint8_t*>(&E[e].x);
+        prefetch_l1(fe);
+        prefetch_l1(fe + 64);
+      }
       const int gsh = E[e].gsh;
       kind = E[e].kind;
 #pragma unroll

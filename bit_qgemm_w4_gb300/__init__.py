@@ -20,7 +20,8 @@ __all__ = [
     "qdequant_w4", "qdequant_w8", "SYMBOLS", "LIB_PATH",
     "SPEC_DTYPE_BF16", "SPEC_DTYPE_F32", "SPEC_QUANT_W4", "SPEC_QUANT_W8",
     "GemmDesc", "GemmStack", "qgemm_stack_create", "qgemm_stack_run", "qgemm_stack_destroy",
-    "spec_set_stream_prefetch", "spec_test_stall",
+    "spec_set_stream_prefetch", "spec_test_stall", "spec_set_gemm_engine",
+    "SPEC_GEMM_ENGINE_AUTO", "SPEC_GEMM_ENGINE_SPLIT", "SPEC_GEMM_ENGINE_STACK",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
@@ -29,6 +30,9 @@ SPEC_DTYPE_BF16 = 0
 SPEC_DTYPE_F32 = 1
 SPEC_QUANT_W4 = 0
 SPEC_QUANT_W8 = 1
+SPEC_GEMM_ENGINE_AUTO = 0
+SPEC_GEMM_ENGINE_SPLIT = 1
+SPEC_GEMM_ENGINE_STACK = 2
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -63,6 +67,7 @@ _SIGS = {
     "qgemm_stack_destroy": [_P],
     "spec_set_stream_prefetch": [_P, _I, _I],
     "spec_test_stall": [_P, _I, _U64],
+    "spec_set_gemm_engine": [_P, _I],
     "qdequant_w4": [_P, _P, _P, _P, _I, _I, _I, _P, _P],
     "qdequant_w8": [_P, _P, _P, _I, _I, _I, _P, _P],
 }
@@ -234,6 +239,10 @@ def spec_set_stream_prefetch(ctx, lead: int, lead_when_full: int) -> None:
 
 def spec_test_stall(ctx, skip_unit: int, wait_limit_ns: int) -> None:
     _call("spec_test_stall", _h(ctx), skip_unit, wait_limit_ns)
+
+
+def spec_set_gemm_engine(ctx, engine: int) -> None:
+    _call("spec_set_gemm_engine", _h(ctx), engine)
 
 
 def fwht_rotate(ctx, x, y, T, K, signs, block, stream=None) -> None:

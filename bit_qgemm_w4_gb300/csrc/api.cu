@@ -100,7 +100,8 @@ namespace {
 
 // Workspace layout (bytes, each region 256-aligned).
 struct WsLayout {
-  size_t err, abort_all, exit_cnt, split_cnt, partials, done, rot_done, xprep, stats, chunks, argidx,
+  size_t err, abort_all, exit_cnt, split_cnt, partials, done, rot_done, tile_counters, split_slots, xprep,
+      stats, chunks, argidx,
       argval, acc_counters, rowstat, rowcnt, gbest, gidx, gsecond, total;
 };
 
@@ -119,6 +120,8 @@ WsLayout layout_for(int num_sms) {
   L.partials = take(sizeof(float) * (size_t)kPartialSlotFloats * kSplitKeys * num_sms);
   L.done = take(sizeof(int) * (size_t)kMaxStack);
   L.rot_done = take(sizeof(int) * (size_t)kMaxStack);
+  L.tile_counters = take(sizeof(int) * 4 * (size_t)kMaxTiles);
+  L.split_slots = take(sizeof(float) * (size_t)kPartialSlotFloats * num_sms);
   L.xprep = take(sizeof(uint16_t) * (size_t)kSplitKeys * kMaxT * kMaxK);
   L.stats = take(sizeof(double) * 2 * (size_t)4096 * kAcceptChunks);
   L.chunks = take(sizeof(double) * kScanBlocks);
@@ -189,10 +192,25 @@ int check_gemm_common(const void* x, const void* y, int y_dtype, int T, int N, i
   return SPEC_OK;
 }
 
+// The split engine: a rotated GEMM is the standalone rotation into the
+// context's scratch, then the GEMM on the rotated bf16 activations; each
+// launch lets the next one start early and waits for its predecessor before
+// it touches what that one wrote.
+int run_split(spec_ctx* ctx, GemmArgs a, cudaStream_t s) {
+  if (a.signs) {
+    SV_TRY(launch_fwht(ctx, a.x, ctx->xprep, a.T, a.K, a.signs, a.rot_block, s));
+    a.x = ctx->xprep;
+    a.signs = nullptr;
+    a.rot_block = 0;
+  }
+  return launch_qgemm_split(ctx, a, s);
+}
+
 int run_gemm(spec_ctx* ctx, GemmArgs& a, void* stream) {
   DeviceGuard dg(ctx->device);
   if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
-  return launch_qgemm(ctx, a, static_cast<cudaStream_t>(stream));
+  if (ctx->engine == SPEC_GEMM_ENGINE_STACK) return launch_qgemm(ctx, a, static_cast<cudaStream_t>(stream));
+  return run_split(ctx, a, static_cast<cudaStream_t>(stream));
 }
 
 // Reads a positive integer tuning knob from the environment (0 if unset).
@@ -251,6 +269,9 @@ int spec_create(int device, size_t workspace_bytes, spec_ctx** out) {
   ctx->partials = reinterpret_cast<float*>(ctx->ws + L.partials);
   ctx->done = reinterpret_cast<int*>(ctx->ws + L.done);
   ctx->rot_done = reinterpret_cast<int*>(ctx->ws + L.rot_done);
+  ctx->tile_counters = reinterpret_cast<int*>(ctx->ws + L.tile_counters);
+  ctx->split_partials = reinterpret_cast<float*>(ctx->ws + L.split_slots);
+  ctx->max_slots = ctx->num_sms;
   if (const int v = env_int("SPEC_PREFETCH_LEAD")) ctx->pf_dist = v;
   if (const int v = env_int("SPEC_PREFETCH_LEAD_FULL")) ctx->pf_max = v;
   ctx->xprep = reinterpret_cast<uint16_t*>(ctx->ws + L.xprep);
@@ -375,6 +396,7 @@ int qgemm_stack_create(spec_ctx* ctx, const spec_gemm_desc* descs, int n, spec_g
     const spec_gemm_desc& d = descs[i];
     GemmArgs a{st->quant, d.qcodes, d.scales, d.zeros, d.group_size, d.x, d.y,
                d.y_dtype == SPEC_DTYPE_F32, d.T, d.N, d.K, d.signs, d.hadamard_block, d.wait_prev};
+    st->args.push_back(a);
     const int rc = build_entry(ctx, a, tpad, i % kSplitKeys, &host[i]);
     if (rc) {
       delete st;
@@ -404,7 +426,19 @@ int qgemm_stack_run(spec_ctx* ctx, const spec_gemm_stack* stack, void* stream) {
   if (stack->ctx != ctx) return set_error(SPEC_ERR_ARG, "stack was created on another context");
   DeviceGuard dg(ctx->device);
   if (!dg.ok) return set_error(SPEC_ERR_CUDA, "cudaSetDevice(%d) failed", ctx->device);
-  return launch_qgemm_stack(ctx, stack, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ctx->engine == SPEC_GEMM_ENGINE_STACK) return launch_qgemm_stack(ctx, stack, s);
+  for (const GemmArgs& a : stack->args) SV_TRY(run_split(ctx, a, s));
+  return SPEC_OK;
+}
+
+int spec_set_gemm_engine(spec_ctx* ctx, int engine) {
+  clear_error();
+  SV_TRY(check_ctx(ctx));
+  if (engine != SPEC_GEMM_ENGINE_AUTO && engine != SPEC_GEMM_ENGINE_SPLIT && engine != SPEC_GEMM_ENGINE_STACK)
+    return set_error(SPEC_ERR_ARG, "engine %d is not SPEC_GEMM_ENGINE_AUTO/SPLIT/STACK", engine);
+  ctx->engine = engine;
+  return SPEC_OK;
 }
 
 int qgemm_stack_destroy(spec_gemm_stack* stack) {

@@ -7,6 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <vector>
 
 #include "specverify.h"
 
@@ -23,6 +24,7 @@ constexpr int kLocalConvStages = 32;         // GEMMs of at most this many stage
                                              // their activations in each CTA's shared memory
 constexpr int kGemmWorkers = 8;              // dequant/epilogue warps per CTA
 constexpr int kMaxStack = 1024;              // GEMMs per stack launch
+constexpr int kMaxTiles = (1 << 22) / kTileM;   // 128-row tiles of the largest N
 constexpr int kMaxAcceptT = 256;
 constexpr int kAcceptChunks = 64;            // max V-chunks per row in the acceptance kernels
 constexpr int kScanBlocks = 256;             // max blocks of the residual scan
@@ -108,6 +110,10 @@ struct spec_ctx {
   size_t ws_bytes = 0;
   uint8_t* ws = nullptr;
   int* err = nullptr;             // device error word
+  int engine = 0;                 // GEMM engine: SPEC_GEMM_ENGINE_* (0 = auto)
+  int* tile_counters = nullptr;   // split engine: [kMaxTiles][4] split-tile arrivals per lane quadrant
+  float* split_partials = nullptr;   // split engine: [max_slots][kPartialSlotFloats] split-tile sums
+  int max_slots = 0;
   float* partials = nullptr;      // [kSplitKeys][num_sms][kPartialSlotFloats] split-tile sums
   int* split_cnt = nullptr;       // [kSplitKeys][num_sms][kGemmWorkers] split-tile arrivals
   int* done = nullptr;            // [kMaxStack] finished tile parts per stack entry
@@ -139,12 +145,14 @@ struct spec_gemm_stack {
   int n = 0;
   int prep_flags = 0;   // kAnyPrep | kAnyConv over the entries
   sv::GemmEntry* dev_entries = nullptr;   // [n] in device memory
+  std::vector<sv::GemmArgs> args;         // [n] the GEMMs as given (split engine)
 };
 
 namespace sv {
 int build_entry(spec_ctx* ctx, const GemmArgs& a, int tpad, int index, GemmEntry* out);
 int gemm_tpad(const GemmArgs& a);   // MMA N of a GEMM: T (2T when rotated) rounded up to 16
 int launch_qgemm(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s);
+int launch_qgemm_split(spec_ctx* ctx, const GemmArgs& a, cudaStream_t s);
 int launch_qgemm_stack(spec_ctx* ctx, const spec_gemm_stack* st, cudaStream_t s);
 int launch_fwht(spec_ctx* ctx, const uint16_t* x, uint16_t* y, int T, int K, const int8_t* signs,
                 int block, cudaStream_t s);

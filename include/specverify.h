@@ -105,18 +105,24 @@ int spec_sync_status(spec_ctx* ctx, void* stream);
  *   y[t][n] = sum_k x'[t][k] * (code[n][k] - zero[k/g][n]) * scale[k/g][n]
  * x' = x, or, when signs != NULL and hadamard_block > 0, the block random
  * Hadamard rotation of x (see fwht_rotate; the weights are taken as stored
- * already rotated).  The rotation runs inside the same launch, in fp32, with
- * one rounding of its result to fp16; signs must then be 16-byte aligned.
+ * already rotated), computed in fp32; signs must then be 16-byte aligned.
  * Sizes: 1 <= T <= 64 (T <= 32 with rotation); N % 32 == 0; K % 64 == 0,
  * K <= 32768; group_size a power of two >= 64 with K % group_size == 0.
  * y_dtype is SPEC_DTYPE_BF16 or SPEC_DTYPE_F32.
- * Numerics: each weight (code - zero) * scale is rounded once to fp16 (the
- * difference is exact, the product rounded); the activations enter the
- * tensor cores as fp16 (bf16 magnitudes from 2^-10 to 65504 convert
- * exactly; smaller ones round to fp16's subnormal grid, larger ones become
- * infinite); the products are summed in fp32.  The result's error is that of the fp16
- * weights, about 1e-3 * RMS(y) at its largest over 10^6 outputs, plus fp32
- * summation and the final rounding of a bf16 output. */
+ * Numerics depend on the context's GEMM engine (spec_set_gemm_engine):
+ *  - split engine (the default): code - zero enters the tensor cores
+ *    exactly (a bf16 integer) with the bf16 activations as given, each 64-k
+ *    group is summed in fp32 and its scale applied in fp32; the result is
+ *    the exact sum up to fp32 rounding.  A rotation is a separate launch on
+ *    the same stream whose result is rounded once to bf16.
+ *  - stack engine: each weight (code - zero) * scale is rounded once to
+ *    fp16 (the difference is exact, the product rounded); the activations
+ *    enter the tensor cores as fp16 (bf16 magnitudes from 2^-10 to 65504
+ *    convert exactly; smaller ones round to fp16's subnormal grid, larger
+ *    ones become infinite); the products are summed in fp32.  The error is
+ *    that of the fp16 weights, about 1e-3 * RMS(y) at its largest over 10^6
+ *    outputs.  A rotation runs inside the same launch, rounded once to fp16.
+ * Either way a bf16 output adds its own final rounding. */
 int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
                 const uint8_t* zeros, int group_size, const uint16_t* x, void* y,
                 int y_dtype, int T, int N, int K, const int8_t* signs,
@@ -128,10 +134,12 @@ int qgemm_w4a16(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
  * scale = scale[n] when group_size == 0, else scale[k/g][n] (group_size a
  * power of two >= 64).  Per-channel scales: the int8 codes enter the tensor
  * cores exactly (bf16 holds -127..127) with the bf16 activations as given,
- * and the scale multiplies the fp32 sum; a rotated activation enters as the
- * sum of two bf16 values (the rounded value and its remainder), so the
- * rotation adds no bf16 rounding.  Grouped scales: code * scale rounded once
- * to fp16 and fp16 activations, as in qgemm_w4a16.  Rotation and sizes as
+ * and the scale multiplies the fp32 sum.  A rotated activation is rounded
+ * once to bf16 (split engine) or enters as the sum of two bf16 values, the
+ * rounded value and its remainder (stack engine, which adds no rounding).
+ * Grouped scales: the split engine sums each 64-k group in fp32 and applies
+ * its scale in fp32; the stack engine rounds code * scale once to fp16 and
+ * takes fp16 activations, as in qgemm_w4a16.  Rotation and sizes as
  * qgemm_w4a16, except N % 8 == 0 suffices and per-channel K may reach 2^20
  * (32768 with rotation). */
 int qgemm_w8a16(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
@@ -164,22 +172,25 @@ typedef struct spec_gemm_desc {
 
 typedef struct spec_gemm_stack spec_gemm_stack;
 
-/* A stack of verify GEMMs run by one persistent launch: the weight pass of
- * the verify step, every projection of every layer in order ("Karpathy's
- * Trick ...", section "Why batch-one decoding is memory-bound": one pass
- * streams every weight once, so the pass is bounded by memory bandwidth).
- * One launch keeps the weight stream running from one GEMM into the next:
- * a GEMM that waits for its predecessors' outputs (wait_prev) waits on the
- * device while the weights after it keep streaming in.
+/* A stack of verify GEMMs: the weight pass of the verify step, every
+ * projection of every layer in order ("Karpathy's Trick ...", section "Why
+ * batch-one decoding is memory-bound": one pass streams every weight once,
+ * so the pass is bounded by memory bandwidth).  With the split engine (the
+ * default) qgemm_stack_run enqueues one launch per GEMM (two for a rotated
+ * one), each GEMM following the previous one as separate calls would; with
+ * the stack engine it is one persistent launch that keeps the weight stream
+ * running from one GEMM into the next: a GEMM that waits for its
+ * predecessors' outputs (wait_prev) waits on the device while the weights
+ * after it keep streaming in.
  * qgemm_stack_create checks and records n descriptors (1 <= n <= 1024); the
  * descriptors' pointers and sizes are fixed from then on (the tensors must
  * stay allocated while the stack is used).  Rules beyond each GEMM's own:
  * one quant for all entries; at most 3 consecutive entries (after the
  * first) with wait_prev = 0.
  * The stack holds a small device array (cudaMalloc at creation) and belongs
- * to `ctx`.  qgemm_stack_run enqueues the whole stack on `stream` (one
- * kernel launch; a launch may be captured in a CUDA graph); the results are
- * those of calling the GEMMs one by one.  qgemm_stack_destroy frees the
+ * to `ctx`.  qgemm_stack_run enqueues the whole stack on `stream` with the
+ * context's current engine (its launches may be captured in a CUDA graph);
+ * the results are those of calling the GEMMs one by one.  qgemm_stack_destroy frees the
  * stack (NULL accepted). */
 int qgemm_stack_create(spec_ctx* ctx, const spec_gemm_desc* descs, int n,
                        spec_gemm_stack** out);
@@ -194,14 +205,33 @@ int qgemm_stack_destroy(spec_gemm_stack* stack);
  * SPEC_PREFETCH_LEAD and SPEC_PREFETCH_LEAD_FULL at spec_create). */
 int spec_set_stream_prefetch(spec_ctx* ctx, int lead, int lead_when_full);
 
+/* The kernel design that runs this context's verify GEMMs (qgemm_w4a16,
+ * qgemm_w8a16, qgemm_stack_run); the results agree within the numerics
+ * stated at qgemm_w4a16.
+ *  SPEC_GEMM_ENGINE_SPLIT: one launch per GEMM, its (tile, 256-k stage)
+ *    units spread evenly over one CTA per SM, a tile cut between CTAs summed
+ *    in fp32 and finished by its last contributor; consecutive launches
+ *    overlap (each starts streaming weights while its predecessor ends).
+ *  SPEC_GEMM_ENGINE_STACK: one persistent launch per call or stack, with
+ *    rotations and activation conversion inside the launch.
+ *  SPEC_GEMM_ENGINE_AUTO (the default): the split engine, which measured
+ *    faster for every workload of the verify step on GB300.
+ * Returns SPEC_ERR_ARG for any other value.  Applies to launches enqueued
+ * after the call. */
+#define SPEC_GEMM_ENGINE_AUTO 0
+#define SPEC_GEMM_ENGINE_SPLIT 1
+#define SPEC_GEMM_ENGINE_STACK 2
+int spec_set_gemm_engine(spec_ctx* ctx, int engine);
+
 /* Test hook for the failure path of the GEMMs' bounded waits (not for
  * production use): the next GEMM launch on this context (qgemm_w4a16,
  * qgemm_w8a16 or qgemm_stack_run) gives every wait a limit of
  * wait_limit_ns (1e5 .. 2e9 ns) instead of the default 2 s, and, when
  * skip_unit >= 0, its CTA 0 never loads the weights of its skip_unit-th
  * stage (if it owns that many), so the waits for that stage run out.  The kernel then records
- * SPEC_ERR_TIMEOUT, stops every CTA, lets its copies and MMAs complete,
- * frees its tensor memory and returns; spec_sync_status reports the error
+ * SPEC_ERR_TIMEOUT, stops (the stack engine: every CTA; the split engine:
+ * the CTAs whose waits run out, while the others finish), lets its copies
+ * and MMAs complete, frees its tensor memory and returns; spec_sync_status reports the error
  * and resets the workspace, after which the context is usable again.  The
  * hook applies to one launch only. */
 int spec_test_stall(spec_ctx* ctx, int skip_unit, uint64_t wait_limit_ns);

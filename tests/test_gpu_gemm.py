@@ -15,12 +15,17 @@ from tests.gpu_util import bf16_dev, dev, gemm_error_ratio, host
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ctx():
+# every test runs under both GEMM engines: one launch per GEMM (split) and
+# the persistent launch (stack)
+@pytest.fixture(scope="module", params=[sv.SPEC_GEMM_ENGINE_SPLIT, sv.SPEC_GEMM_ENGINE_STACK],
+                ids=["split", "stack"])
+def ctx(request):
     import torch  # noqa: F401
     from bit_qgemm_w4_gb300 import build
     build.build()
     c = sv.Context(0)
+    sv.spec_set_gemm_engine(c, request.param)
+    c.engine = request.param
     yield c
     c.close()
 

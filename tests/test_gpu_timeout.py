@@ -20,12 +20,17 @@ pytestmark = pytest.mark.gpu
 SPEC_ERR_TIMEOUT = -6
 
 
-@pytest.fixture(scope="module")
-def ctx():
+# every test runs under both GEMM engines: one launch per GEMM (split) and
+# the persistent launch (stack)
+@pytest.fixture(scope="module", params=[sv.SPEC_GEMM_ENGINE_SPLIT, sv.SPEC_GEMM_ENGINE_STACK],
+                ids=["split", "stack"])
+def ctx(request):
     import torch  # noqa: F401
     from bit_qgemm_w4_gb300 import build
     build.build()
     c = sv.Context(0)
+    sv.spec_set_gemm_engine(c, request.param)
+    c.engine = request.param
     yield c
     c.close()
 
@@ -59,8 +64,10 @@ def test_single_gemm_wait_runs_out_and_context_recovers(ctx, skip_unit):
 
 
 def test_stack_wait_runs_out_and_context_recovers(ctx):
-    # a stalled CTA also leaves the other CTAs waiting at the next GEMM's
-    # dependency gate; the grid-wide abort flag releases them
+    # stack engine: a stalled CTA also leaves the other CTAs waiting at the
+    # next GEMM's dependency gate, and the grid-wide abort flag releases
+    # them; split engine: the hook stalls the first GEMM's launch, the
+    # later launches run to their end
     import torch
     rng = np.random.default_rng(8100)
     T, dims = 16, [1024, 2048, 1024, 2048]
@@ -71,7 +78,9 @@ def test_stack_wait_runs_out_and_context_recovers(ctx):
               "zeros": dev(W.zeros), "group_size": 64, "x": bf16_dev(x), "y": y, "T": T, "N": W.N,
               "K": W.K, "wait_prev": 1} for W, x, y in zip(Ws, xs, ys)]
     st = sv.GemmStack(ctx, descs)
-    sv.spec_test_stall(ctx, 1, 5_000_000)
+    # a stage CTA 0 owns: the split engine's first launch gives it one
+    skip = 0 if ctx.engine == sv.SPEC_GEMM_ENGINE_SPLIT else 1
+    sv.spec_test_stall(ctx, skip, 5_000_000)
     st.run()
     with pytest.raises(sv.SpecError) as e:
         sv.spec_sync_status(ctx)

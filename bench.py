@@ -13,16 +13,19 @@ generator; they exceed L2, so no step reuses another's cached weights.
 Printed: one JSON line.  `value` is algorithmic HBM bytes per step / device
 time per step (GB/s) with inputs resident; `e2e` is the same metric when
 every step also copies its inputs from pinned host memory (double-buffered
-against the previous step's compute) and reads its result back.  Sub-objects
-time, each on its own graph: `t16` (the stack at T = 16 without head and
-acceptance), `t16_unfused` (seven GEMMs per layer), `per_gemm_launches`
-(one launch per GEMM), `w4_rot32` (the T = 32 stack with the block-32
+against the previous step's compute) and reads its result back.  The GEMMs
+run on the engine `--engine` names (default: the split engine, one launch
+per GEMM); `stack_engine` times the step's GEMM stack and the 27B-class
+stack on the persistent engine for comparison.  Sub-objects time, each on
+its own graph: `t16` (the stack at T = 16 without head and acceptance),
+`t16_unfused` (seven GEMMs per layer), `per_gemm_launches` (one
+qgemm_w4a16 call per GEMM), `w4_rot32` (the T = 32 stack with the block-32
 rotation), `w8_27b` (the 27B-class int8 stack with rotation),
-`accept_gumbel` (shared-seed acceptance of the same blocks) and `accept_tree`
-(greedy trees of 1 to 64 nodes).  `--impl reference` times the fp64 CPU
-oracle on a bounded sample instead; `--kernel-case`, `--kernel-case-w8`,
-`--stack-case`, `--accept-case`, `--gumbel-case` and `--tree-case` time one
-kernel alone.
+`accept_gumbel` (shared-seed acceptance of the same blocks) and
+`accept_tree` (greedy trees of 1 to 64 nodes).  `--impl reference` times the
+fp64 CPU oracle on a bounded sample instead; `--kernel-case`,
+`--kernel-case-w8`, `--stack-case`, `--accept-case`, `--gumbel-case` and
+`--tree-case` time one kernel alone.
 """
 from __future__ import annotations
 
@@ -164,8 +167,19 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "bit_qgemm_w4_gb300", "csrc", "qgemm.cu")
+ENGINES = {"auto": 0, "split": 1, "stack": 2}   # SPEC_GEMM_ENGINE_*
+
+
+def open_ctx(args, device: int):
+    """A context on `device` whose GEMMs run on the engine --engine names."""
+    import bit_qgemm_w4_gb300 as sv
+    ctx = sv.Context(device)
+    sv.spec_set_gemm_engine(ctx, ENGINES[args.engine])
+    return ctx
+
+
+def kernel_source_hash(name: str = "qgemm_split.cu") -> str:
+    p = os.path.join(ROOT, "bit_qgemm_w4_gb300", "csrc", name)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
@@ -179,7 +193,8 @@ def ncu_traffic(key: str):
         d = json.load(open(p)).get(key)
     except Exception:
         return None
-    if not d or d.get("qgemm_cu_sha256_16") != kernel_source_hash():
+    src = d.get("source") if d else None
+    if not src or d.get("source_sha256_16") != kernel_source_hash(src):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -256,7 +271,7 @@ def run_gpu(args):
     svbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    ctx = sv.Context(local)
+    ctx = open_ctx(args, local)
     gen = torch.Generator(device=dev)
     gen.manual_seed(20240 + rank)
 
@@ -517,6 +532,15 @@ def run_gpu(args):
     w8_ms = time_graph(g_w8, K8)
     w8n_ms = time_graph(g_w8n, K8)
     w8_bytes = inputs.LAYERS_27B * sum(w8_gemm_bytes(T_MAIN, N, K) for _, K, N in L8)
+    # ---- the other engine on the same T=32 stack and 27B rotated stack
+    other = "stack" if ENGINES[args.engine] != ENGINES["stack"] else "split"
+    sv.spec_set_gemm_engine(ctx, ENGINES[other])
+    g_o32 = graph_of(st32.run)
+    o32_ms = time_graph(g_o32, max(5, min(K, 20)))
+    g_o8 = graph_of(st8.run)
+    o8_ms = time_graph(g_o8, K8)
+    sv.spec_set_gemm_engine(ctx, ENGINES[args.engine])
+    del g_o32, g_o8
     del g_w8, g_w8n, st8, st8n, w8
     clocks = sampler.stop()
     sv.spec_sync_status(ctx)
@@ -600,6 +624,7 @@ def run_gpu(args):
     ms_per_step = total_ms / K
     nbytes = step_bytes()
     gemm_bytes = stack_bytes(T_MAIN) + head_bytes(T_MAIN)
+    n_gemm = inputs.LAYERS_9B * len(inputs.LAYER_9B) + 1   # GEMM launches per step (split engine)
     peak, peak_kind = hbm_peak()
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
     accepted = []
@@ -634,9 +659,14 @@ def run_gpu(args):
                 "acceptance_levels": list(ACCEPT_LEVELS),
                 "l2": "inputs larger than L2 (4.08 GB of weights per step)",
                 "parallelism": f"replicas x{world}",
-                "graph": "one CUDA graph per step part: the GEMM stack (one persistent launch of "
-                         "all 145 GEMMs, each waiting for its predecessor) and the acceptance "
-                         "(two launches)",
+                "engine": args.engine,
+                "graph": ("one CUDA graph per step part: the GEMM stack (145 launches, one per "
+                          "GEMM, each starting its weight stream while its predecessor ends and "
+                          "reading its activations once that one has finished)"
+                          if ENGINES[args.engine] != ENGINES["stack"] else
+                          "one CUDA graph per step part: the GEMM stack (one persistent launch of "
+                          "all 145 GEMMs, each waiting for its predecessor)") +
+                         " and the acceptance (two launches)",
             },
             "pct_of_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
             "draft_tokens_scored_per_s": round(world * T_MAIN / (ms_per_step * 1e-3), 1),
@@ -668,7 +698,7 @@ def run_gpu(args):
             },
             "t16": {
                 "workload": "same 36-layer int4 stack at T=16 (no head, no acceptance), one stack "
-                            "launch",
+                            "run",
                 "ms_per_step": round(t16_ms, 5),
                 "value": round(stack_bytes(T_SMALL) / (t16_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
@@ -677,17 +707,17 @@ def run_gpu(args):
             },
             "t16_unfused": {
                 "workload": "the T=16 stack as the configuration states it: q, k, v, o, gate, up, "
-                            "down as 7 GEMMs per layer (252 GEMMs, one stack launch; k, v and up "
-                            "do not wait for the GEMM before them)",
+                            "down as 7 GEMMs per layer (252 GEMMs, one stack run; on the stack "
+                            "engine k, v and up do not wait for the GEMM before them)",
                 "ms_per_step": round(unf_ms, 5),
                 "value": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
                 "frac": round(stack_bytes(T_SMALL) / (unf_ms * 1e-3) / 1e9 / peak, 4),
             },
             "w4_rot32": {
-                "workload": "the T=32 verify GEMM stack (36 layers + LM head, one launch) with the "
-                            "block-32 random Hadamard rotation of every GEMM's activations inside "
-                            "the launch",
+                "workload": "the T=32 verify GEMM stack (36 layers + LM head) with the block-32 "
+                            "random Hadamard rotation of every GEMM's activations (split engine: "
+                            "a rotation launch before each GEMM; stack engine: inside the launch)",
                 "ms_per_step": round(r32_ms, 5),
                 "value": round(gemm_bytes / (r32_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s",
@@ -698,8 +728,8 @@ def run_gpu(args):
             "w8_27b": {
                 "workload": "27B-class int8 per-channel stack at T=32: 64 layers (qkv 5120x7168, "
                             "o 5120x5120, gate_up 5120x34816, down 17408x5120), block-1024 random "
-                            "Hadamard rotation of every GEMM's activations inside the launch (no "
-                            "head, no acceptance)",
+                            "Hadamard rotation of every GEMM's activations (no head, no "
+                            "acceptance)",
                 "ms_per_step": round(w8_ms, 5),
                 "bytes_per_step": w8_bytes,
                 "value": round(w8_bytes / (w8_ms * 1e-3) / 1e9, 2),
@@ -709,15 +739,31 @@ def run_gpu(args):
                 "without_rotation_ms": round(w8n_ms, 5),
                 "rotation_overhead": round(w8_ms / w8n_ms - 1.0, 4),
             },
+            "stack_engine" if other == "stack" else "split_engine": {
+                "workload": f"the same T=32 verify GEMM stack and 27B-class int8 rotated stack on "
+                            f"the {other} engine",
+                "t32_ms": round(o32_ms, 5),
+                "t32_value": round(gemm_bytes / (o32_ms * 1e-3) / 1e9, 2),
+                "t32_frac": round(gemm_bytes / (o32_ms * 1e-3) / 1e9 / peak, 4),
+                "w8_27b_ms": round(o8_ms, 5),
+                "w8_27b_value": round(w8_bytes / (o8_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
+            },
             "roofline": {
-                "kernel": "qgemm_kernel<W4, TPAD=32> (one launch: the step's 145 GEMMs)",
+                "kernel": ("qgemm_split_kernel<W4, TPAD=32> (the step's 145 GEMM launches; "
+                           "bytes and time are their sums)"
+                           if ENGINES[args.engine] != ENGINES["stack"] else
+                           "qgemm_kernel<W4, TPAD=32> (one launch: the step's 145 GEMMs)"),
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                 "peak_source": f"{peak_kind} HBM copy bandwidth" +
                                (" (of fallback)" if peak_kind == "fallback" else " (of measured)"),
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": ncu_traffic("qgemm_w4_t32_verify_step"),
+                "traffic": ncu_traffic("qgemm_w4_t32_verify_step"
+                                       if ENGINES[args.engine] != ENGINES["stack"] else
+                                       "qgemm_w4_t32_verify_step_stack_engine"),
                 "bytes_per_launch": gemm_bytes,
                 "launch_ms": round(gemm_ms, 6),
+                "launches_per_step": 1 if ENGINES[args.engine] == ENGINES["stack"] else n_gemm,
             },
             "cpu_baseline": cpu,
             "e2e": {
@@ -727,7 +773,7 @@ def run_gpu(args):
                 "staging": "double-buffered device inputs: step i+1's host-to-device copy runs on a "
                            "copy stream while step i computes; every step reads its result back",
             },
-            "gpu_launches": K * 3,
+            "gpu_launches": K * ((1 if ENGINES[args.engine] == ENGINES["stack"] else n_gemm) + 2),
             "clocks": clocks,
         }
         print(json.dumps(out), flush=True)
@@ -878,7 +924,7 @@ def run_kernel_case(args):
     svbuild.build()
     T, N, K = (int(v) for v in args.kernel_case.split(","))
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     # enough distinct matrices that consecutive launches do not hit in L2
@@ -919,7 +965,7 @@ def run_kernel_case_w8(args):
     T, N, K = vals[:3]
     B = vals[3] if len(vals) > 3 else 0
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(9)
     copies = max(1, min(16, (256 << 20) // max(1, N * K) + 1))
@@ -961,7 +1007,7 @@ def run_fwht_case(args):
     svbuild.build()
     T, K, B = [int(v) for v in args.fwht_case.split(",")]
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(13)
     x = inputs.activations_device(gen, T, K, dev)
@@ -999,7 +1045,7 @@ def run_stack_case(args):
     svbuild.build()
     name, _, depth = args.stack_case.partition(":")
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     gen = torch.Generator(device=dev)
     gen.manual_seed(11)
     descs, keep, nbytes = [], [], 0
@@ -1088,7 +1134,7 @@ def run_accept_case(args):
     svbuild.build()
     T, V = (int(v) for v in args.accept_case.split(","))
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     a = inputs.accept_inputs(np.random.default_rng(11), T, V, logit_std=3.0, alpha=1.0, noise_std=0.5)
     logits = torch.from_numpy(a.logits).to(dev)
     q = torch.from_numpy(a.q).to(dev)
@@ -1126,7 +1172,7 @@ def run_gumbel_case(args):
     svbuild.build()
     T, V = (int(v) for v in args.gumbel_case.split(","))
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     a = inputs.accept_inputs(np.random.default_rng(11), T, V, logit_std=3.0, alpha=1.0, noise_std=0.5)
     logits = torch.from_numpy(a.logits).to(dev)
     logq = torch.from_numpy(np.log(a.q).astype(np.float32)).to(dev)
@@ -1165,7 +1211,7 @@ def run_tree_case(args):
     svbuild.build()
     T, V = (int(v) for v in args.tree_case.split(","))
     dev = torch.device("cuda", 0)
-    ctx = sv.Context(0)
+    ctx = open_ctx(args, 0)
     tin = inputs.tree_inputs(np.random.default_rng(500 + T), T, V, logit_std=3.0, p_match=0.7)
     logits = torch.from_numpy(tin.logits).to(dev)
     d = torch.from_numpy(tin.drafts).to(dev)
@@ -1197,6 +1243,9 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--engine", default="auto", choices=sorted(ENGINES),
+                    help="GEMM engine: split (one launch per GEMM; auto), stack (one persistent "
+                         "launch per call or stack)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle GEMM work in the CPU baseline sample")

@@ -1,5 +1,6 @@
-// Verify GEMM for the speculative-decoding verification step: low-bit weights
-// times the T drafted positions' activations, on the sm_103a tensor cores.
+// The stack engine of the verify GEMM (selected with spec_set_gemm_engine;
+// the default split engine is in qgemm_split.cu): low-bit weights times the
+// T drafted positions' activations, on the sm_103a tensor cores.
 //
 // What it computes ("Karpathy's Trick for Faster Local LLMs Finally Has Proper
 // Tooling", section "How Uzu optimizes bytes and tokens per pass": 4-bit

@@ -1,11 +1,14 @@
-// Verify GEMM for the speculative-decoding verification step: low-bit weights
-// times the T drafted positions' activations, on the sm_103a tensor cores.
+// The split engine of the verify GEMM (the default; the persistent engine is
+// in qgemm.cu): one launch per GEMM, low-bit weights times the T drafted
+// positions' activations, on the sm_103a tensor cores.
 //
 // What it computes ("Karpathy's Trick for Faster Local LLMs Finally Has Proper
 // Tooling", section "How Uzu optimizes bytes and tokens per pass": 4-bit
 // asymmetric Medium tier, 8-bit symmetric Large tier, one scale per group):
 //   y[t][n] = sum_k x[t][k] * (code[n][k] - zero[g][n]) * scale[g][n]   (int4)
 //   y[t][n] = sum_k x[t][k] *  code[n][k]              * scale         (int8)
+// A rotated GEMM reads activations that the standalone rotation kernel
+// wrote just before it on the same stream.
 //
 // Design (swap-AB: 128 weight rows are the MMA's M dimension, the T drafted
 // positions its N dimension; one CTA per SM owns all 512 TMEM columns):
@@ -39,6 +42,8 @@
 //    its ring with weights while that GEMM's last CTAs finish.
 // Every wait is bounded (see ptx.cuh); a timeout records an error, drains the
 // CTA's in-flight copies/MMAs and frees its tensor memory before returning.
+// A test hook (spec_test_stall) shortens the limit and withholds one stage's
+// weights from CTA 0 for one launch.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -216,7 +221,7 @@ __device__ __forceinline__ void dequant_w8(uint32_t row_addr, uint32_t m, int j,
 
 template <int QUANT, int TPAD>
 __global__ void __launch_bounds__(Cfg<QUANT, TPAD>::kThreads, 1)
-    qgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
+    qgemm_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_codes,
                  const __grid_constant__ CUtensorMap tm_scales,
                  const __grid_constant__ CUtensorMap tm_zeros, const Params p) {
   using C = Cfg<QUANT, TPAD>;
@@ -664,7 +669,7 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   static std::atomic<uint32_t> attr_done{0};   // per instantiation, one bit per device
   const uint32_t bit = ctx->device < 32 ? (1u << ctx->device) : 0u;
   if (!bit || !(attr_done.load() & bit)) {
-    rc = check_cuda(cudaFuncSetAttribute(qgemm_kernel<QUANT, TPAD>,
+    rc = check_cuda(cudaFuncSetAttribute(qgemm_split_kernel<QUANT, TPAD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes),
                     "cudaFuncSetAttribute(qgemm)");
@@ -682,7 +687,7 @@ int launch_t(spec_ctx* ctx, const GemmArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return check_cuda(cudaLaunchKernelEx(&cfg, qgemm_kernel<QUANT, TPAD>, tx, tc, ts, tz, p), "qgemm launch");
+  return check_cuda(cudaLaunchKernelEx(&cfg, qgemm_split_kernel<QUANT, TPAD>, tx, tc, ts, tz, p), "qgemm_split launch");
 }
 
 template <int QUANT>

@@ -22,6 +22,7 @@ __all__ = [
     "GemmDesc", "GemmStack", "qgemm_stack_create", "qgemm_stack_run", "qgemm_stack_destroy",
     "spec_set_stream_prefetch", "spec_test_stall", "spec_set_gemm_engine",
     "SPEC_GEMM_ENGINE_AUTO", "SPEC_GEMM_ENGINE_SPLIT", "SPEC_GEMM_ENGINE_STACK",
+    "spec_repack_w4_codes",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
@@ -70,6 +71,7 @@ _SIGS = {
     "spec_set_gemm_engine": [_P, _I],
     "qdequant_w4": [_P, _P, _P, _P, _I, _I, _I, _P, _P],
     "qdequant_w8": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "spec_repack_w4_codes": [_P, _P, _I, _I],
 }
 SYMBOLS = tuple(_SIGS)
 
@@ -296,3 +298,11 @@ def qdequant_w4(ctx, qcodes, scales, zeros, group_size, N, K, w, stream=None) ->
 def qdequant_w8(ctx, qcodes, scales, group_size, N, K, w, stream=None) -> None:
     _call("qdequant_w8", _h(ctx), _ptr(qcodes), _ptr(scales), group_size, N, K, _ptr(w),
           _stream(stream))
+
+
+def spec_repack_w4_codes(src, dst, N: int, K: int) -> None:
+    """Host arrays (numpy uint8, C-contiguous, N*K/2 bytes each); dst may be src."""
+    for a in (src, dst):
+        if not (a.flags["C_CONTIGUOUS"] and a.dtype.itemsize == 1 and a.size == N * K // 2):
+            raise ValueError("src and dst must be C-contiguous byte arrays of N*K/2 bytes")
+    _call("spec_repack_w4_codes", src.ctypes.data, dst.ctypes.data, N, K)

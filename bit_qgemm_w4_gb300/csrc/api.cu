@@ -634,4 +634,21 @@ int qdequant_w8(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales, int
                         static_cast<cudaStream_t>(stream));
 }
 
+int spec_repack_w4_codes(const uint8_t* src, uint8_t* dst, int N, int K) {
+  clear_error();
+  if (!src || !dst) return set_error(SPEC_ERR_ARG, "src or dst is null");
+  if (N < 1 || K < 8 || K % 8) return set_error(SPEC_ERR_SHAPE, "N=%d K=%d: need N >= 1, K >= 8, K %% 8 == 0", N, K);
+  const size_t groups = (size_t)N * (size_t)(K / 8);
+  for (size_t i = 0; i < groups; ++i) {
+    // plain order: s0 = (k0, k1), s1 = (k2, k3), s2 = (k4, k5), s3 = (k6, k7) as (low, high)
+    const uint32_t s0 = src[4 * i], s1 = src[4 * i + 1], s2 = src[4 * i + 2], s3 = src[4 * i + 3];
+    // library order: (k0, k2), (k4, k6), (k1, k3), (k5, k7)
+    dst[4 * i] = (uint8_t)((s0 & 0xFu) | ((s1 & 0xFu) << 4));
+    dst[4 * i + 1] = (uint8_t)((s2 & 0xFu) | ((s3 & 0xFu) << 4));
+    dst[4 * i + 2] = (uint8_t)((s0 >> 4) | (s1 & 0xF0u));
+    dst[4 * i + 3] = (uint8_t)((s2 >> 4) | (s3 & 0xF0u));
+  }
+  return SPEC_OK;
+}
+
 }  // extern "C"

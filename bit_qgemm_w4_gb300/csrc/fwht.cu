@@ -1,9 +1,10 @@
 // Standalone block-diagonal random Hadamard rotation of bf16 activations
 // (fwht_rotate).  The transform of one (row, block) is fwht_warp (fwht.cuh):
 // "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling",
-// section "How Uzu optimizes bytes and tokens per pass".  The verify GEMMs
-// rotate their activations inside their own launch; this kernel serves
-// callers that want the rotated activations themselves.
+// section "How Uzu optimizes bytes and tokens per pass".  The split GEMM
+// engine runs it before each rotated GEMM (the stack engine rotates inside
+// its own launch); it also serves callers that want the rotated activations
+// themselves.
 
 #include "fwht.cuh"
 #include "internal.hpp"

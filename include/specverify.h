@@ -373,6 +373,17 @@ int qdequant_w4(spec_ctx* ctx, const uint8_t* qcodes, const uint16_t* scales,
 int qdequant_w8(spec_ctx* ctx, const int8_t* qcodes, const uint16_t* scales,
                 int group_size, int N, int K, float* w, void* stream);
 
+/* Checkpoint conversion, on the host (no context, no GPU, no stream): int4
+ * codes packed in plain order -- byte i of row n holds k = 2i in its low
+ * nibble and k = 2i + 1 in its high nibble, uint8 [N][K/2] -- rewritten in
+ * this library's int4 code layout (see "Storage layouts" above).  Every 4
+ * source bytes (8 consecutive k) map to the same 4 destination bytes, so dst
+ * may equal src (in place); any other overlap is not allowed.  src and dst
+ * are host pointers of N * K / 2 bytes owned by the caller.  Returns
+ * SPEC_ERR_ARG for a null pointer, SPEC_ERR_SHAPE unless N >= 1, K >= 8 and
+ * K % 8 == 0. */
+int spec_repack_w4_codes(const uint8_t* src, uint8_t* dst, int N, int K);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,9 +5,10 @@
 // stop at the first rejection, draw the replacement from the normalised
 // positive part of p - q; if every draft is accepted the target supplies one
 // more token.  Tree rule ("Karpathy's Trick for Faster Local LLMs Finally Has
-// Proper Tooling", section "Issue with parallel draft generation"): verify the
-// tree and keep the longest valid path -- here greedily, a node is valid when
-// its token is the target's argmax for the row that scores it.
+// Proper Tooling", section "Issue with parallel draft generation"): the target
+// scores every node of the draft tree in one pass, and of the root paths whose
+// nodes it confirms the deepest one is emitted -- here greedily, the target
+// confirms a node when its token is the argmax of the row that scores it.
 //
 // Launch structure (two launches for the chain rule, one for the tree):
 //  * row_stats_kernel: grid (chunks, rows); each block reduces one V-chunk of

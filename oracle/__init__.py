@@ -20,11 +20,11 @@ argmax) standing in for a step where the definition is plain.  Sources:
   group-shared scales; block-diagonal random Hadamard transform with sign
   flips before the mixing, +/-1 entries and one overall scale.  Sections
   "Producing several tokens from one model pass" and "Issue with parallel
-  draft generation": verify several positions / a tree in one pass and keep
-  the longest valid path.
+  draft generation": one target pass scores several positions or a whole
+  draft tree; of the root paths the target confirms, the deepest is emitted.
 * "Local LLM 4x Faster--Not Through Hardware, but Through Speculative
-  Decoding" (wink.run): random Hadamard transform for outliers; tree verify
-  accepting the longest path.
+  Decoding" (wink.run): random Hadamard transform for outliers; a tree of
+  drafts checked in one pass, its deepest confirmed path emitted.
 * The trymirai post feed (nitterts.pages.dev/trymirai), the post on the
   "random number from 1 to 10" example: the speculator and the target both
   sample with the same seed through the Gumbel-max trick, so matching

@@ -4,7 +4,7 @@ Sources: "Speculative Decoding Clearly Explained" (the cat-sat walkthrough,
 bonus token, distribution preservation) and "Karpathy's Trick for Faster
 Local LLMs Finally Has Proper Tooling", sections "Producing several tokens
 from one model pass" (five drafts, four agree, advance five) and "Issue with
-parallel draft generation" (tree, longest valid path).
+parallel draft generation" (a draft tree, its deepest confirmed path).
 """
 import itertools
 import json

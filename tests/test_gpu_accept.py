@@ -225,3 +225,30 @@ def test_fwht_parity(ctx):
         ref = oracle.rht(oracle.bf16_bits_to_f64(xb), s, B)
         err = np.abs(host(y) - ref)
         assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.sqrt(np.mean(ref ** 2))), B
+
+
+@pytest.mark.parametrize("aligned", [True, False])
+def test_fwht_block32_in_place_any_sign_alignment(ctx, aligned):
+    # block 32 (the split engine's rotation before each block-32 GEMM) at an
+    # odd T, with 16-byte aligned and unaligned signs, out of place and in
+    # place, against the oracle
+    import torch
+    from tests.gpu_util import bf16_dev
+    rng = np.random.default_rng(12 + aligned)
+    T, K = 33, 4096
+    xb = inputs.activations(rng, T, K)
+    s = inputs.hadamard_signs(rng, K)
+    sbuf = torch.zeros(K + 16, dtype=torch.int8, device="cuda")
+    off = 0 if aligned else 1
+    sbuf[off:off + K] = torch.from_numpy(s).to("cuda")
+    sig = sbuf[off:off + K]
+    assert (sig.data_ptr() % 16 == 0) == aligned
+    ref = oracle.rht(oracle.bf16_bits_to_f64(xb), s, 32)
+    y = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    sv.fwht_rotate(ctx, bf16_dev(xb), y, T, K, sig, 32)
+    xin = bf16_dev(xb)
+    sv.fwht_rotate(ctx, xin, xin, T, K, sig, 32)
+    torch.cuda.synchronize()
+    for out in (host(y), host(xin)):
+        err = np.abs(out - ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.sqrt(np.mean(ref ** 2)))

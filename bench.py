@@ -841,6 +841,7 @@ def cpu_oracle_leg(layer, xl, head, x_head, acc_sets, kept, budget_s):
               f"step's {step_bytes() / 1e9:.2f} GB; {dt:.1f} s; numpy BLAS threads for the matmul, "
               f"the rest single-threaded")
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "threads": {"blas_matmul": os.cpu_count(), "everything_else": 1},
             "kind": "oracle", "sample": sample,
             "parity": {"gemm_max_err_over_bar": round(worst, 4), "gemm_pass": worst <= 1.0,
                        "accept": acc,
@@ -907,6 +908,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": WORKLOAD, "T": T_MAIN, "sample": sample},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                         "threads": {"blas_matmul": os.cpu_count(), "everything_else": 1},
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -397,7 +397,10 @@ def run_gpu(args):
     total_ms = evs[0][0].elapsed_time(evs[K - 1][2])
     gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     acc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    step_ms_med = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+    step_times = sorted(e[0].elapsed_time(e[2]) for e in evs)
+    step_ms_med = statistics.median(step_times)
+    step_ms_p10 = step_times[int(0.1 * (len(step_times) - 1))]
+    step_ms_p90 = step_times[int(round(0.9 * (len(step_times) - 1)))]
     sv.spec_sync_status(ctx)
 
     # outputs of the last timed step, kept for the CPU-oracle leg's comparison
@@ -671,6 +674,8 @@ def run_gpu(args):
             "pct_of_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
             "draft_tokens_scored_per_s": round(world * T_MAIN / (ms_per_step * 1e-3), 1),
             "verify_step_ms_median": round(step_ms_med, 5),
+            "verify_step_ms_p10": round(step_ms_p10, 5),
+            "verify_step_ms_p90": round(step_ms_p90, 5),
             "acceptance_ms": round(acc_ms, 5),
             "acceptance_share": round(acc_ms / (gemm_ms + acc_ms), 4),
             "accepted": accepted,
